@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of one training step of the head-chunked attention layer.
+
+One step = upipe_attn_fwd + upipe_attn_bwd of a GQA/RoPE causal attention
+layer (projections, RoPE, attention, output projection; forward and
+backward with per-chunk recomputation) on synthetic bf16 inputs resident in
+HBM.  Default workload: the Llama-3-8B layer shape (L=32768, D=4096, H=32,
+Hkv=8, d=128) with U=8 query heads per chunk.
+
+Prints one JSON line.  `value` is the layer's algorithmic TFLOP/s (causal
+attention fwd+bwd 7*L^2*H*d plus the projections' 3*(2*L*D*(H+2Hkv)*d +
+2*L*H*d*D); the backward recomputation is hardware work and is not counted)
+over the device-timed steps.  `--impl reference` times the fp64 CPU oracle
+on the same metric instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s (% BF16 peak) at 1 GB300; peak activation bytes vs U"
+
+WORKLOADS = {
+    "llama3_8b_layer_L32768_U8": dict(L=32768, D=4096, H=32, Hkv=8, U=8),
+    "tiny_L1024_U2": dict(L=1024, D=1024, H=8, Hkv=2, U=2),
+    "qwen32b_layer_L131072_U8": dict(L=131072, D=5120, H=64, Hkv=8, U=8),
+    "llama3_8b_layer_L65536_U4": dict(L=65536, D=4096, H=32, Hkv=8, U=4),
+}
+DEFAULT = "llama3_8b_layer_L32768_U8"
+
+
+def layer_flops(L, D, H, Hkv, d=128):
+    attn = 7.0 * L * L * H * d
+    proj = 3.0 * (2.0 * L * D * (H + 2 * Hkv) * d + 2.0 * L * H * d * D)
+    return attn, proj
+
+
+def kernel_flops(kind, w, d=128):
+    """Algorithmic flops of one launch of `kind` in the layer path."""
+    L, D, H, Hkv, U = w["L"], w["D"], w["H"], w["Hkv"], w["U"]
+    g = H // Hkv
+    kvc = U // g if U >= g else 1
+    slots = U + 2 * kvc
+    tri = L * L / 2.0  # causal (query, key) pairs per head
+    return {
+        "attn_fwd": 2 * 2 * tri * U * d,        # S = QK^T, O = PV
+        "attn_bwd_dkdv": 4 * 2 * tri * U * d,   # S^T, dP^T, dV, dK
+        "attn_bwd_dq": 3 * 2 * tri * U * d,     # S, dP, dQ
+        "qkv_gemm": 2.0 * L * slots * d * D,
+        "oproj_gemm": 2.0 * L * U * d * D,
+        "do_gemm": 2.0 * L * U * d * D,
+        "dwo_gemm": 2.0 * L * U * d * D,
+        "dwqkv_gemm": 2 * 2.0 * L * slots * d * D,  # high and low halves
+        "dx_gemm": 2 * 2.0 * L * slots * d * D,
+    }.get(kind)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return m.get("bf16_tflops", 1900.0), m.get("bf16_tflops_sustained", 1700.0), m.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(L):
+    """Times the fp64 oracle on one query head (H = Hkv = 1) of causal
+    attention fwd+bwd at sequence length L; returns (TFLOP/s, seconds)."""
+    import numpy as np
+    from headwise_chunked_context_gb300 import synth
+    from oracle import upipe_oracle as orc
+    q, k, v, do = synth.core_inputs(L, 1, 1)
+    q, k, v, do = (t.double().numpy() for t in (q, k, v, do))
+    t0 = time.perf_counter()
+    o, lse = orc.attention_core_fwd(q, k, v)
+    orc.attention_core_bwd(q, k, v, o, lse, do)
+    dt = time.perf_counter() - t0
+    return 7.0 * L * L * 128 / dt / 1e12, dt
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    L_sample = args.ref_sample_L
+    for _ in range(args.warmup):
+        cpu_oracle_sample(L_sample)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, s = cpu_oracle_sample(L_sample)
+        vals.append(v)
+        secs.append(s)
+    value = statistics.mean(vals)
+    cores = os.cpu_count()
+    sample = (f"fp64 NumPy oracle, one query head (H=Hkv=1, d=128) of causal attention fwd+bwd at "
+              f"L={L_sample} per step, standing in for the {args.workload} workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **w},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def source_sha(name):
+    p = os.path.join(ROOT, "headwise_chunked_context_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+KIND_SOURCE = {"attn_fwd": "attn_fwd.cu", "attn_bwd_dq": "attn_bwd.cu", "attn_bwd_dkdv": "attn_bwd.cu"}
+
+
+def traffic_for(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        t = json.load(f)
+    e = t.get(kind)
+    if not e or e.get("workload") != workload:
+        return None
+    src = KIND_SOURCE.get(kind, "gemm.cu")
+    if e.get("source_sha") != source_sha(src):
+        return None
+    return e.get("bytes_per_launch")
+
+
+def run_upipe(args, w, world, rank, local):
+    from headwise_chunked_context_gb300 import upipe, build
+    if not os.path.exists(upipe.LIB_PATH):
+        build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L, D, H, Hkv, U = w["L"], w["D"], w["H"], w["Hkv"], w["U"]
+    cfg = upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=U)
+    stream = torch.cuda.current_stream(dev)
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+    x = torch.randn((L, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    wqkv = (torch.randn(((H + 2 * Hkv) * 128, D), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    wo = (torch.randn((D, H * 128), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    dout = torch.randn((L, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    out = torch.empty((L, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, L), dtype=torch.float32, device=dev)
+    dx = torch.empty((L, D), dtype=torch.bfloat16, device=dev)
+    dwqkv = torch.empty(((H + 2 * Hkv) * 128, D), dtype=torch.float32, device=dev)
+    dwo = torch.empty((D, H * 128), dtype=torch.float32, device=dev)
+    ws_bytes = max(upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+
+    def step():
+        upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
+        upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code = upipe.last_device_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {upipe.strerror(code)}")
+
+    # ---- timed region: K steps, device events, clocks sampled throughout
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = upipe.launch_count()
+    upipe.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    upipe.profile_enable(False)
+    launches = upipe.launch_count() - n0
+    barrier()
+    ms = e0.elapsed_time(e1)
+    prof = upipe.profile_read()
+    clocks = clk.summary()
+    code = upipe.last_device_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after timed steps: {upipe.strerror(code)}")
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    peak_alloc = torch.cuda.max_memory_allocated(dev) - base_alloc
+
+    attn_f, proj_f = layer_flops(L, D, H, Hkv)
+    step_flops = attn_f + proj_f
+    ms_step = ms / args.steps
+    value = world * step_flops / (ms_step / 1e3) / 1e12
+    burst, sustained, hbm, peak_src = peaks()
+
+    # ---- roofline of the dominant kernel, from the live per-launch events
+    busy = {k: v for k, v in prof.items() if v[1] > 0}
+    dom = max(busy, key=lambda k: busy[k][0])
+    dom_ms, dom_n = busy[dom]
+    fl = kernel_flops(dom, w)
+    achieved = fl / (dom_ms / dom_n / 1e3) / 1e12
+    traffic = traffic_for(dom, args.workload)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                "frac": achieved / sustained, "traffic": traffic, "kernel": dom,
+                "peak_kind": f"bf16 sustained ({peak_src})"}
+    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps,
+                   "share": v[0] / sum(x[0] for x in busy.values())} for k, v in busy.items()}
+    for k in kernels:
+        f = kernel_flops(k, w)
+        if f:
+            kernels[k]["tflops"] = f / (busy[k][0] / busy[k][1] / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = lambda t: t.to("cpu").pin_memory()
+        hx, hw, hwo, hd = pin(x), pin(wqkv), pin(wo), pin(dout)
+        ho, hl, hdx, hdw, hdwo = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                                  for t in (out, lse, dx, dwqkv, dwo))
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hwo, hd))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdx, hdw, hdwo))
+        k_e2e = max(1, min(args.steps, 3))
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            wqkv.copy_(hw, non_blocking=True)
+            wo.copy_(hwo, non_blocking=True)
+            dout.copy_(hd, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            hdx.copy_(dx, non_blocking=True)
+            hdw.copy_(dwqkv, non_blocking=True)
+            hdwo.copy_(dwo, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a0.elapsed_time(a1) / k_e2e
+        e2e = {"value": world * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---- activation accounting vs U
+    act = {}
+    for u in sorted({U, H}):
+        c = upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=u)
+        fb, ff = upipe.activation_bytes(c, 0)
+        bb, bf = upipe.activation_bytes(c, 1)
+        act[f"U={u}"] = {"chunk_bytes_fwd": fb, "chunk_bytes_bwd": bb, "fixed_bytes_bwd": bf,
+                         "workspace_bwd": upipe.workspace_bytes(c, 1)}
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, s = cpu_oracle_sample(L)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 NumPy oracle, one query head (H=Hkv=1) of causal attention fwd+bwd at L={L}, "
+                         f"{s:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, **w, "d": 128, "rope_theta": 500000.0, "causal": True,
+                   "o_saved": False, "flops_per_step": step_flops, "attn_flops_per_step": attn_f,
+                   "l2": "inputs larger than L2 (x, dout 256 MiB each at L=32768)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_bf16_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
+                          "peaks": f"{burst}/{sustained} TFLOP/s ({peak_src})"},
+        "attn_core_tflops": world * attn_f / (sum(busy[k][0] for k in ("attn_fwd", "attn_bwd_dq", "attn_bwd_dkdv")
+                                                  if k in busy) / args.steps / 1e3) / 1e12,
+        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks, "activation_bytes": act, "peak_alloc_bytes_in_step": peak_alloc,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="upipe", choices=["upipe", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-sample-L", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    world, rank, local = (1, 0, 0)
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, w, world, rank)
+        return
+    world, rank, local = dist_setup()
+    try:
+        run_upipe(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,318 @@
+// Exact causal attention forward for one head-chunk, tcgen05 + TMEM.
+//
+// What it computes: for query head h with KV head h / g, S = Q K^T / sqrt(d)
+// with keys j <= i visible to query i, O = softmax(S) V and
+// LSE_i = ln sum_j exp(S_ij).  The method keeps this formula unchanged and
+// only changes which heads are resident at a time ("Untied Ulysses Pushes
+// Llama-3-8B Training to 5 Million Tokens", paragraph on intermediate
+// buffers: "not a new attention formula, but a different memory schedule").
+//
+// Design (sm_103a):
+//  * one CTA = one 128-query tile of one head; CTAs are launched heaviest
+//    (most KV blocks) first so the causal triangle balances across SMs;
+//  * warp 4 streams Q once and K/V blocks of 128 keys through a two-stage
+//    TMA ring (128-byte swizzle);
+//  * warp 5 issues tcgen05.mma from one thread: S = Q K^T into one of two
+//    TMEM score buffers while the softmax warps work on the other, then
+//    O += P V into a TMEM accumulator;
+//  * warps 0-3 own one query row per thread (the TMEM lane), so the row max
+//    and row sum are thread-local.  They write P as bf16 into a swizzled
+//    shared tile (the A operand of the P V product).  O is rescaled in TMEM
+//    only when a row maximum grows by more than 2^8, which keeps every
+//    exponent bounded and the result exact up to rounding.
+#include "sm103_ptx.cuh"
+
+namespace upipe {
+namespace {
+
+constexpr int kTile = 128 * 128 * 2;  // [128][128] bf16, stored as two 64-column halves
+constexpr int kHalf = kTile / 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + kTile;      // 2 stages
+constexpr int OFF_V = OFF_K + 2 * kTile;  // 2 stages
+constexpr int OFF_P = OFF_V + 2 * kTile;  // 2 buffers
+constexpr int OFF_BAR = OFF_P + 2 * kTile;
+
+enum {
+  B_Q_FULL,
+  B_K_FULL,     // +2
+  B_K_EMPTY = B_K_FULL + 2,
+  B_V_FULL = B_K_EMPTY + 2,
+  B_V_EMPTY = B_V_FULL + 2,
+  B_S_FULL = B_V_EMPTY + 2,
+  B_S_EMPTY = B_S_FULL + 2,
+  B_P_FULL = B_S_EMPTY + 2,
+  B_P_EMPTY = B_P_FULL + 2,
+  B_PV_DONE = B_P_EMPTY + 2,
+  B_DRAIN,
+  B_COUNT
+};
+constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
+constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
+constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;  // + alignment slack
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int TM_S = 0;    // two score buffers: columns [0,128) and [128,256)
+constexpr int TM_O = 256;  // O accumulator: [256, 384)
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ AttnFwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // heaviest tiles first
+  const int h = blockIdx.y;
+  const int kz = p.k_z0 + h / p.g_loc;
+  const int vz = p.v_z0 + h / p.g_loc;
+  const int n_kv = qb + 1;  // causal: KV blocks 0..qb
+  auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  const WaitCtl w{abort_flag, p.status, p.limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_K_FULL + s), 1);
+      mbar_init(bar(B_K_EMPTY + s), 1);
+      mbar_init(bar(B_V_FULL + s), 1);
+      mbar_init(bar(B_V_EMPTY + s), 1);
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_S_EMPTY + s), 4);
+      mbar_init(bar(B_P_FULL + s), 4);
+      mbar_init(bar(B_P_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(sb + OFF_TMEM_SLOT, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&mq);
+      tma_prefetch_map(&mk);
+      tma_prefetch_map(&mv);
+      mbar_expect_tx(bar(B_Q_FULL), kTile);
+      tma_load_3d(sb + OFF_Q, &mq, bar(B_Q_FULL), 0, qb * 128, p.q_z0 + h);
+      tma_load_3d(sb + OFF_Q + kHalf, &mq, bar(B_Q_FULL), 64, qb * 128, p.q_z0 + h);
+      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(bar(B_K_EMPTY + s), ph ^ 1, w)) break;
+        mbar_expect_tx(bar(B_K_FULL + s), kTile);
+        tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, j * 128, kz);
+        tma_load_3d(sb + OFF_K + s * kTile + kHalf, &mk, bar(B_K_FULL + s), 64, j * 128, kz);
+        last_k[s] = j;
+        if (!mbar_wait(bar(B_V_EMPTY + s), ph ^ 1, w)) break;
+        mbar_expect_tx(bar(B_V_FULL + s), kTile);
+        tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, j * 128, vz);
+        tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, j * 128, vz);
+        last_v[s] = j;
+      }
+      if (*abort_flag) {  // let every issued copy land before the CTA exits
+        mbar_wait_drain(bar(B_Q_FULL), 0, p.status);
+        for (int s = 0; s < 2; ++s) {
+          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] >> 1) & 1, p.status);
+          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] >> 1) & 1, p.status);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
+      constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
+      auto issue_pv = [&](int jj) -> bool {
+        const int s = jj & 1;
+        const uint32_t ph = (jj >> 1) & 1;
+        if (!mbar_wait(bar(B_P_FULL + s), ph, w)) return false;
+        if (!mbar_wait(bar(B_V_FULL + s), ph, w)) return false;
+        tc_fence_after();
+        const uint32_t pa = sb + OFF_P + s * kTile;
+        const uint32_t va = sb + OFF_V + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(va + kk * 2048, kHalf, 1024);
+          umma_bf16(tmem + TM_O, a, b, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_P_EMPTY + s));
+        umma_commit(bar(B_V_EMPTY + s));
+        umma_commit(bar(B_PV_DONE));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_Q_FULL), 0, w);
+      tc_fence_after();
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!(ok = mbar_wait(bar(B_K_FULL + s), ph, w))) break;
+        if (!(ok = mbar_wait(bar(B_S_EMPTY + s), ph ^ 1, w))) break;
+        tc_fence_after();
+        const uint32_t ka = sb + OFF_K + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + TM_S + s * 128, sdesc_sw128(sb + OFF_Q + off, 16, 1024),
+                    sdesc_sw128(ka + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_S_FULL + s));
+        umma_commit(bar(B_K_EMPTY + s));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(n_kv - 1);
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = warp * 32 + lane;  // query row in the tile = TMEM lane
+    const int qpos = qb * 128 + r;
+    const uint32_t trow = tmem_lane_addr(tmem, warp, 0);
+    const float sl2 = p.scale_log2;
+    float m_use = -INFINITY;  // running max used as the exponent offset (log2 domain)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!(ok = warp_wait(bar(B_S_FULL + s), ph, w))) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tmem_ld32(trow + TM_S + s * 128 + 0, v0);
+      tmem_ld32(trow + TM_S + s * 128 + 32, v1);
+      tmem_ld32(trow + TM_S + s * 128 + 64, v2);
+      tmem_ld32(trow + TM_S + s * 128 + 96, v3);
+      tmem_ld_wait(v0);
+      tmem_ld_wait(v1);
+      tmem_ld_wait(v2);
+      tmem_ld_wait(v3);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + s));
+
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        x[c] = __uint_as_float(v0[c]);
+        x[32 + c] = __uint_as_float(v1[c]);
+        x[64 + c] = __uint_as_float(v2[c]);
+        x[96 + c] = __uint_as_float(v3[c]);
+      }
+      if (j == qb) {  // diagonal block: key c visible iff c <= r
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > r) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = fmaxf(m_use, mx * sl2);
+      const bool need = m_new > m_use + 8.0f;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O holds PV(0..j-1): wait for PV(j-1), then rescale the rows that moved.
+        if (!(ok = warp_wait(bar(B_PV_DONE), (j - 1) & 1, w))) break;
+        tc_fence_after();
+        const float f = need ? ex2_approx(m_use - m_new) : 1.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(trow + TM_O + c4 * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+          tmem_st32(trow + TM_O + c4 * 32, o);
+        }
+        tmem_st_wait();
+        l *= f;
+      }
+      if (need) m_use = m_new;
+
+      uint32_t pk[64];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2_approx(fmaf(x[c], sl2, -m_use));
+        const float p1 = ex2_approx(fmaf(x[c + 1], sl2, -m_use));
+        rs += p0 + p1;
+        pk[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+
+      if (!(ok = warp_wait(bar(B_P_EMPTY + s), ph ^ 1, w))) break;
+      const uint32_t pa = sb + OFF_P + s * kTile;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        st_shared_v4(pa + (ch >> 3) * kHalf + sw128_offset(r, ch & 7), pk[4 * ch], pk[4 * ch + 1],
+                     pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P_FULL + s));
+    }
+    if (ok) ok = warp_wait(bar(B_PV_DONE), (n_kv - 1) & 1, w);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = qpos < p.L;
+      __nv_bfloat16* orow = p.o + static_cast<int64_t>(qpos) * p.o_row + static_cast<int64_t>(h) * p.o_head;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + c4 * 32, o);
+        tmem_ld_wait(o);
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            st_global_v4(orow + c4 * 32 + q * 8,
+                         pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+          }
+        }
+      }
+      if (valid && p.write_lse)
+        p.lse[static_cast<int64_t>(h) * p.L + qpos] = (m_use + log2f(l)) * 0.69314718055994530942f;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const AttnFwdParams& p, int n_qblocks, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_qblocks, p.nheads);
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace upipe

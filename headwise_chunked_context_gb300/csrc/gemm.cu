@@ -1,0 +1,387 @@
+// tcgen05 GEMM for the chunk-sliced projections of the attention layer.
+//
+// The layer's Q, K, V, O matrices and their projections ("the query, key,
+// and value matrices in the transformer layer", talk write-up "Untied
+// Ulysses Pushes Llama-3-8B Training to 5 Million Tokens", Q&A paragraph)
+// are sliced per head-chunk: a chunk only ever materialises its own heads'
+// rows of Q/K/V and its own share of the output projection, accumulated
+// into a carried partial result (same write-up, paragraph on intermediate
+// buffers: "a partial result is stored").
+//
+// Kernel shape: one CTA per 128x128 output tile, K in blocks of 64 bf16
+// (one 128-byte swizzle row), a 3-stage TMA ring, one thread issuing
+// tcgen05.mma (M=128, N=128, K=16) into a 128-column TMEM accumulator,
+// four epilogue warps reading the accumulator back one row per thread.
+// Operands are K-major (rows of 64 contiguous K) or MN-major (rows of
+// contiguous M/N, two 64-wide boxes per tile); both use the same swizzled
+// shared layout and differ only in the descriptor.
+//
+// Fixed reduction order: every output element accumulates its K blocks in
+// ascending order inside TMEM; a carried fp32 partial (out32 / dx32) is
+// loaded into TMEM before the first MMA so that chunked and unchunked runs
+// perform the same fp32 additions in the same order.
+#include "sm103_ptx.cuh"
+
+namespace upipe {
+namespace {
+
+constexpr int kTile = 128 * 64 * 2;  // one 16 KB operand tile (128 x 64 bf16)
+
+// Shared-memory layout per kind.  The weight-gradient and dx GEMMs read the
+// layer's dQ/dK/dV as a pair of bf16 tensors (value and rounding residual)
+// and accumulate both products, which keeps ~16 significant bits of the
+// fp32 gradients through the sum over tokens.
+template <int KIND>
+struct Layout {
+  static constexpr bool kSplit = (KIND == GK_DWQKV || KIND == GK_DX);
+  static constexpr int kStages = kSplit ? 2 : 3;
+  static constexpr int kA = kSplit ? 2 * kTile : kTile;
+  static constexpr int kStage = kA + kTile;
+  static constexpr int OFF_BAR = kStages * kStage;
+  static constexpr int B_FULL = 0;
+  static constexpr int B_EMPTY = kStages;
+  static constexpr int B_ACC_FULL = 2 * kStages;
+  static constexpr int B_ACC_READY = 2 * kStages + 1;
+  static constexpr int B_DRAIN = 2 * kStages + 2;
+  static constexpr int B_COUNT = 2 * kStages + 3;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
+  static constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
+};
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 128;
+
+template <int KIND>
+struct Traits;
+template <> struct Traits<GK_QKV>   { static constexpr int a_mn = 0, b_mn = 0; };
+template <> struct Traits<GK_OPROJ> { static constexpr int a_mn = 0, b_mn = 0; };
+template <> struct Traits<GK_DO>    { static constexpr int a_mn = 0, b_mn = 1; };
+template <> struct Traits<GK_DWO>   { static constexpr int a_mn = 1, b_mn = 1; };
+template <> struct Traits<GK_DWQKV> { static constexpr int a_mn = 1, b_mn = 1; };
+template <> struct Traits<GK_DX>    { static constexpr int a_mn = 0, b_mn = 1; };
+
+template <int KIND>
+__device__ __forceinline__ void load_a(const CUtensorMap* m, const GemmParams& p, uint32_t dst, uint32_t bar,
+                                       int mt, int kb) {
+  if constexpr (KIND == GK_QKV || KIND == GK_DO) {
+    tma_load_2d(dst, m, bar, kb * 64, mt * 128);
+  } else if constexpr (KIND == GK_OPROJ) {
+    tma_load_2d(dst, m, bar, p.a_col0 + kb * 64, mt * 128);
+  } else if constexpr (KIND == GK_DWO) {
+    tma_load_2d(dst, m, bar, mt * 128, kb * 64);
+    tma_load_2d(dst + 8192, m, bar, mt * 128 + 64, kb * 64);
+  } else if constexpr (KIND == GK_DWQKV) {
+    const int z = p.tab0[mt];
+    tma_load_3d(dst, m, bar, 0, kb * 64, z);
+    tma_load_3d(dst + 8192, m, bar, 64, kb * 64, z);
+    tma_load_3d(dst + kTile, m, bar, 0, kb * 64, z + p.lo_z);
+    tma_load_3d(dst + kTile + 8192, m, bar, 64, kb * 64, z + p.lo_z);
+  } else {  // GK_DX
+    const int z = p.tab0[kb >> 1];
+    tma_load_3d(dst, m, bar, (kb & 1) * 64, mt * 128, z);
+    tma_load_3d(dst + kTile, m, bar, (kb & 1) * 64, mt * 128, z + p.lo_z);
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void load_b(const CUtensorMap* m, const GemmParams& p, uint32_t dst, uint32_t bar,
+                                       int nt, int kb) {
+  if constexpr (KIND == GK_QKV) {
+    tma_load_2d(dst, m, bar, kb * 64, p.tab0[nt] * 128);
+  } else if constexpr (KIND == GK_OPROJ) {
+    tma_load_2d(dst, m, bar, p.b_col0 + kb * 64, nt * 128);
+  } else if constexpr (KIND == GK_DO || KIND == GK_DWO || KIND == GK_DWQKV) {
+    tma_load_2d(dst, m, bar, p.b_col0 + nt * 128, kb * 64);
+    tma_load_2d(dst + 8192, m, bar, p.b_col0 + nt * 128 + 64, kb * 64);
+  } else {  // GK_DX
+    const int row = p.tab1[kb >> 1] * 128 + (kb & 1) * 64;
+    tma_load_2d(dst, m, bar, nt * 128, row);
+    tma_load_2d(dst + 8192, m, bar, nt * 128 + 64, row);
+  }
+}
+
+template <int MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+  if constexpr (MN) return sdesc_sw128(base + kk * 2048, 8192, 1024);
+  else return sdesc_sw128(base + kk * 32, 16, 1024);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+                const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  using Lt = Layout<KIND>;
+  constexpr int kStages = Lt::kStages;
+  constexpr int OFF_BAR = Lt::OFF_BAR;
+  constexpr int B_FULL = Lt::B_FULL, B_EMPTY = Lt::B_EMPTY, B_ACC_FULL = Lt::B_ACC_FULL;
+  constexpr int B_ACC_READY = Lt::B_ACC_READY, B_DRAIN = Lt::B_DRAIN;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // N tiles vary fastest so that CTAs resident together share the A row block.
+  const int nt = blockIdx.x;
+  const int mt = blockIdx.y;
+  auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lt::OFF_ABORT);
+  const WaitCtl w{abort_flag, p.status, p.limit_ns};
+  constexpr bool kCarry = (KIND == GK_OPROJ || KIND == GK_DX);
+  const bool carry_in = kCarry && p.carry_in;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_ACC_FULL), 1);
+    mbar_init(bar(B_ACC_READY), 4);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + Lt::OFF_TMEM_SLOT, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lt::OFF_TMEM_SLOT);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&ma);
+      tma_prefetch_map(&mb);
+      int last[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last[s] = -1;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        if (!mbar_wait(bar(B_EMPTY + s), ph ^ 1, w)) break;
+        const uint32_t dst = sb + s * Lt::kStage;
+        mbar_expect_tx(bar(B_FULL + s), Lt::kStage);
+        load_a<KIND>(&ma, p, dst, bar(B_FULL + s), mt, kb);
+        load_b<KIND>(&mb, p, dst + Lt::kA, bar(B_FULL + s), nt, kb);
+        last[s] = kb;
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < kStages; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar(B_FULL + s), (last[s] / kStages) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, 128, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
+      bool ok = true;
+      if (carry_in) {
+        ok = mbar_wait(bar(B_ACC_READY), 0, w);
+        tc_fence_after();
+      }
+      for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        if (!(ok = mbar_wait(bar(B_FULL + s), ph, w))) break;
+        tc_fence_after();
+        const uint32_t a = sb + s * Lt::kStage;
+        const uint32_t b = a + Lt::kA;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16(tmem, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(b, kk), idesc,
+                    (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
+        }
+        if constexpr (Lt::kSplit) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem, operand_desc<Traits<KIND>::a_mn>(a + kTile, kk), operand_desc<Traits<KIND>::b_mn>(b, kk),
+                      idesc, 1u);
+        }
+        umma_commit(bar(B_EMPTY + s));
+      }
+      if (ok) umma_commit(bar(B_ACC_FULL));
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int m = mt * 128 + r;
+    const bool valid = m < p.M;
+    const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
+    bool ok = true;
+
+    if constexpr (kCarry) {
+      if (carry_in) {
+        const float* crow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint4 t = valid ? ld_global_nc_v4(crow + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
+            v[4 * q] = t.x;
+            v[4 * q + 1] = t.y;
+            v[4 * q + 2] = t.z;
+            v[4 * q + 3] = t.w;
+          }
+          tmem_st32(trow + c4 * 32, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ACC_READY));
+      }
+    }
+
+    ok = warp_wait(bar(B_ACC_FULL), 0, w);
+    if (ok) {
+      tc_fence_after();
+      if constexpr (KIND == GK_QKV) {
+        const int slot = nt;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
+        const bool rot = slot < p.rope_slots;
+        const float2* tab = p.rope + static_cast<int64_t>(m) * 64;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32], b[32];
+          tmem_ld32(trow + half * 32, a);
+          tmem_ld32(trow + 64 + half * 32, b);
+          tmem_ld_wait(a);
+          tmem_ld_wait(b);
+          float lo[32], hi[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x0 = __uint_as_float(a[i]);
+            const float x1 = __uint_as_float(b[i]);
+            if (rot && valid) {
+              const float2 cs = tab[half * 32 + i];
+              lo[i] = x0 * cs.x - x1 * cs.y;
+              hi[i] = x0 * cs.y + x1 * cs.x;
+            } else {
+              lo[i] = x0;
+              hi[i] = x1;
+            }
+          }
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              st_global_v4(orow + half * 32 + q * 8, pack_bf16x2(lo[8 * q], lo[8 * q + 1]),
+                           pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]), pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]),
+                           pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
+              st_global_v4(orow + 64 + half * 32 + q * 8, pack_bf16x2(hi[8 * q], hi[8 * q + 1]),
+                           pack_bf16x2(hi[8 * q + 2], hi[8 * q + 3]), pack_bf16x2(hi[8 * q + 4], hi[8 * q + 5]),
+                           pack_bf16x2(hi[8 * q + 6], hi[8 * q + 7]));
+            }
+          }
+        }
+      } else if constexpr (KIND == GK_DO) {
+        const int slot = nt;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
+        const __nv_bfloat16* obf = p.o_rows + static_cast<int64_t>(m) * p.ld_o + slot * kHeadDim;
+        float dsum = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(trow + c4 * 32, v);
+          tmem_ld_wait(v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              st_global_v4(orow + c4 * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              const uint4 ov = ld_global_nc_v4(obf + c4 * 32 + q * 8);
+              const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                dsum = fmaf(bf16_lo(pk[4 * q + e]), bf16_lo(ow[e]), dsum);
+                dsum = fmaf(bf16_hi(pk[4 * q + e]), bf16_hi(ow[e]), dsum);
+              }
+            }
+          }
+        }
+        if (valid) p.delta[static_cast<int64_t>(slot) * p.L + m] = dsum;
+      } else {
+        // fp32 or carried outputs: OPROJ, DX (carry / final bf16), DWO, DWQKV (fp32).
+        float* frow = nullptr;
+        __nv_bfloat16* brow = nullptr;
+        if constexpr (kCarry) {
+          if (p.final_out)
+            brow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(m) * p.ld_out + nt * 128;
+          else
+            frow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
+        } else if constexpr (KIND == GK_DWO) {
+          frow = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ld_out + p.out_col0 + nt * 128;
+        } else {  // GK_DWQKV
+          frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(trow + c4 * 32, v);
+          tmem_ld_wait(v);
+          if (valid) {
+            if (brow) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                st_global_v4(brow + c4 * 32 + q * 8,
+                             pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                             pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                             pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                             pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                st_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t s) {
+  constexpr int smem = Layout<KIND>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_tiles, p.m_tiles);
+  gemm_kernel<KIND><<<grid, kThreads, smem, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        cudaStream_t s) {
+  switch (kind) {
+    case GK_QKV: return launch_kind<GK_QKV>(a, b, p, s);
+    case GK_OPROJ: return launch_kind<GK_OPROJ>(a, b, p, s);
+    case GK_DO: return launch_kind<GK_DO>(a, b, p, s);
+    case GK_DWO: return launch_kind<GK_DWO>(a, b, p, s);
+    case GK_DWQKV: return launch_kind<GK_DWQKV>(a, b, p, s);
+    case GK_DX: return launch_kind<GK_DX>(a, b, p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace upipe

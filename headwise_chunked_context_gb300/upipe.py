@@ -1,0 +1,295 @@
+"""Thin ctypes binding of libupipe.so (declared in include/upipe.h).
+
+Argument marshalling only: torch tensors are checked for dtype, shape,
+device and contiguity, then their device pointers and the current CUDA
+stream are handed to the C entry points of the same names.  Every step of
+the attention layer runs in the library's sm_103a kernels; there is no
+fallback path, and a missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libupipe.so")
+
+UPIPE_OK = 0
+UPIPE_ERR_INVALID_ARG = -1
+UPIPE_ERR_WS_TOO_SMALL = -2
+UPIPE_ERR_CUDA = -3
+UPIPE_ERR_DEVICE_TIMEOUT = -4
+UPIPE_ERR_UNSUPPORTED_DEVICE = -5
+
+EXPORTS = (
+    "upipe_workspace_bytes",
+    "upipe_activation_bytes",
+    "upipe_attn_fwd",
+    "upipe_attn_bwd",
+    "upipe_attn_core_fwd",
+    "upipe_attn_core_bwd",
+    "upipe_last_device_status",
+    "upipe_debug_wait_timeout",
+    "upipe_launch_count",
+    "upipe_profile_enable",
+    "upipe_profile_read",
+    "upipe_strerror",
+)
+
+KINDS = ("rope_table", "qkv_gemm", "attn_fwd", "oproj_gemm", "do_gemm", "dwo_gemm", "attn_bwd_dq",
+         "attn_bwd_dkdv", "dwqkv_gemm", "dx_gemm", "delta")
+
+
+class UpipeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+class Cfg(ctypes.Structure):
+    """Mirror of ``upipe_cfg``."""
+
+    _fields_ = [
+        ("L", ctypes.c_int64),
+        ("D", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("U", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("rope_theta", ctypes.c_double),
+    ]
+
+
+@dataclass(frozen=True)
+class Config:
+    L: int
+    H: int
+    Hkv: int
+    U: int
+    D: int = 0
+    d: int = 128
+    rope_theta: float = 500000.0
+    causal: int = 1
+
+    def c(self) -> Cfg:
+        return Cfg(self.L, self.D, self.H, self.Hkv, self.d, self.U, self.causal, self.rope_theta)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Opens libupipe.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with headwise_chunked_context_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        cfgp = ctypes.POINTER(Cfg)
+        L.upipe_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_workspace_bytes.argtypes = [cfgp, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.upipe_activation_bytes.restype = ctypes.c_int
+        L.upipe_activation_bytes.argtypes = [cfgp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+        L.upipe_attn_fwd.restype = ctypes.c_int
+        L.upipe_attn_fwd.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_bwd.restype = ctypes.c_int
+        L.upipe_attn_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_core_fwd.restype = ctypes.c_int
+        L.upipe_attn_core_fwd.argtypes = [cfgp, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_core_bwd.restype = ctypes.c_int
+        L.upipe_attn_core_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_last_device_status.restype = ctypes.c_int
+        L.upipe_last_device_status.argtypes = [P]
+        L.upipe_debug_wait_timeout.restype = ctypes.c_int
+        L.upipe_debug_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.upipe_launch_count.restype = ctypes.c_int64
+        L.upipe_launch_count.argtypes = []
+        L.upipe_profile_enable.restype = None
+        L.upipe_profile_enable.argtypes = [ctypes.c_int]
+        L.upipe_profile_read.restype = ctypes.c_int
+        L.upipe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.c_int]
+        L.upipe_strerror.restype = ctypes.c_char_p
+        L.upipe_strerror.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().upipe_strerror(code).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != UPIPE_OK:
+        raise UpipeError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _expect(t, shape, dtype, name):
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+
+
+# ----------------------------------------------------------- raw entry points
+
+def workspace_bytes(cfg: Config, pass_: int, core_only: bool = False, has_o_saved: bool = False) -> int:
+    c = cfg.c()
+    return int(lib().upipe_workspace_bytes(ctypes.byref(c), pass_, int(core_only), int(has_o_saved)))
+
+
+def activation_bytes(cfg: Config, pass_: int, core_only: bool = False, has_o_saved: bool = False):
+    c = cfg.c()
+    chunk = ctypes.c_size_t(0)
+    fixed = ctypes.c_size_t(0)
+    _check(lib().upipe_activation_bytes(ctypes.byref(c), pass_, int(core_only), int(has_o_saved),
+                                        ctypes.byref(chunk), ctypes.byref(fixed)), "upipe_activation_bytes")
+    return int(chunk.value), int(fixed.value)
+
+
+def _ws(cfg, pass_, core_only, has_o_saved, ws, device):
+    need = workspace_bytes(cfg, pass_, core_only, has_o_saved)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def attn_fwd(cfg: Config, x, Wqkv, Wo, out, lse, o_saved=None, ws=None, stream=None):
+    L, D, H, Hkv = cfg.L, cfg.D, cfg.H, cfg.Hkv
+    _expect(x, (L, D), torch.bfloat16, "x")
+    _expect(Wqkv, ((H + 2 * Hkv) * 128, D), torch.bfloat16, "Wqkv")
+    _expect(Wo, (D, H * 128), torch.bfloat16, "Wo")
+    _expect(out, (L, D), torch.bfloat16, "out")
+    _expect(lse, (H, L), torch.float32, "lse")
+    if o_saved is not None:
+        _expect(o_saved, (L, H * 128), torch.bfloat16, "o_saved")
+    ws, nbytes = _ws(cfg, 0, False, o_saved is not None, ws, x.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_fwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(out), _ptr(lse),
+                                _ptr(o_saved), _ptr(ws), nbytes, _stream(stream)), "upipe_attn_fwd")
+
+
+def attn_bwd(cfg: Config, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved=None, ws=None, stream=None):
+    L, D, H, Hkv = cfg.L, cfg.D, cfg.H, cfg.Hkv
+    _expect(dout, (L, D), torch.bfloat16, "dout")
+    _expect(dx, (L, D), torch.bfloat16, "dx")
+    _expect(dWqkv, ((H + 2 * Hkv) * 128, D), torch.float32, "dWqkv")
+    _expect(dWo, (D, H * 128), torch.float32, "dWo")
+    _expect(lse, (H, L), torch.float32, "lse")
+    ws, nbytes = _ws(cfg, 1, False, o_saved is not None, ws, x.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_bwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(dout), _ptr(lse),
+                                _ptr(o_saved), _ptr(dx), _ptr(dWqkv), _ptr(dWo), _ptr(ws), nbytes,
+                                _stream(stream)), "upipe_attn_bwd")
+
+
+def attn_core_fwd(cfg: Config, q, k, v, o, lse, ws=None, stream=None):
+    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
+    _expect(q, (L, H, 128), torch.bfloat16, "q")
+    _expect(k, (L, Hkv, 128), torch.bfloat16, "k")
+    _expect(v, (L, Hkv, 128), torch.bfloat16, "v")
+    _expect(o, (L, H, 128), torch.bfloat16, "o")
+    _expect(lse, (H, L), torch.float32, "lse")
+    need = workspace_bytes(cfg, 0, True)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if need and ws is None:
+        ws, nbytes = _ws(cfg, 0, True, False, None, q.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_core_fwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                     _ptr(ws), nbytes, _stream(stream)), "upipe_attn_core_fwd")
+
+
+def attn_core_bwd(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, ws=None, stream=None):
+    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
+    for t, shp, n in ((do, (L, H, 128), "dout_o"), (dq, (L, H, 128), "dq"), (dk, (L, Hkv, 128), "dk"),
+                      (dv, (L, Hkv, 128), "dv")):
+        _expect(t, shp, torch.bfloat16, n)
+    ws, nbytes = _ws(cfg, 1, True, False, ws, q.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_core_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream)),
+           "upipe_attn_core_bwd")
+
+
+def last_device_status(stream=None) -> int:
+    return int(lib().upipe_last_device_status(_stream(stream)))
+
+
+def debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(lib().upipe_debug_wait_timeout(limit_ns, _stream(stream)), "upipe_debug_wait_timeout")
+
+
+def launch_count() -> int:
+    return int(lib().upipe_launch_count())
+
+
+def profile_enable(on: bool) -> None:
+    lib().upipe_profile_enable(int(on))
+
+
+def profile_read():
+    """{kind: (total ms, launches)} for launches recorded since the last read."""
+    n = len(KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    lib().upipe_profile_read(ms, cnt, n)
+    return {KINDS[k]: (float(ms[k]), int(cnt[k])) for k in range(n)}
+
+
+# ------------------------------------------------------- allocating helpers
+
+def layer_forward(cfg: Config, x, Wqkv, Wo, keep_o: bool = False):
+    """Allocates out [L, D] bf16, lse [H, L] fp32 (and O if keep_o) and runs
+    upipe_attn_fwd.  Returns (out, lse, o_saved or None)."""
+    dev = x.device
+    out = torch.empty((cfg.L, cfg.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((cfg.H, cfg.L), dtype=torch.float32, device=dev)
+    o_saved = torch.empty((cfg.L, cfg.H * 128), dtype=torch.bfloat16, device=dev) if keep_o else None
+    attn_fwd(cfg, x, Wqkv, Wo, out, lse, o_saved)
+    return out, lse, o_saved
+
+
+def layer_backward(cfg: Config, x, Wqkv, Wo, dout, lse, o_saved=None):
+    """Allocates dx [L, D] bf16, dWqkv, dWo fp32 and runs upipe_attn_bwd."""
+    dev = x.device
+    dx = torch.empty((cfg.L, cfg.D), dtype=torch.bfloat16, device=dev)
+    dWqkv = torch.empty(((cfg.H + 2 * cfg.Hkv) * 128, cfg.D), dtype=torch.float32, device=dev)
+    dWo = torch.empty((cfg.D, cfg.H * 128), dtype=torch.float32, device=dev)
+    attn_bwd(cfg, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved)
+    return dx, dWqkv, dWo
+
+
+def core_forward(cfg: Config, q, k, v):
+    o = torch.empty_like(q)
+    lse = torch.empty((cfg.H, cfg.L), dtype=torch.float32, device=q.device)
+    attn_core_fwd(cfg, q, k, v, o, lse)
+    return o, lse
+
+
+def core_backward(cfg: Config, q, k, v, o, lse, do):
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    attn_core_bwd(cfg, q, k, v, o, lse, do, dq, dk, dv)
+    return dq, dk, dv

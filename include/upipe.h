@@ -1,0 +1,191 @@
+/*
+ * upipe.h -- C ABI of the head-chunked GQA/RoPE causal attention layer
+ * (UPipe, "Untied Ulysses") for one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * One attention layer of a Llama-style transformer, computed one chunk of U
+ * query heads at a time over the full sequence:
+ *
+ *   "Untied Ulysses: Memory-Efficient Context Parallelism via Headwise
+ *   Chunking" (index page, Abstract): fine-grained chunking at the attention
+ *   head level, reducing intermediate tensor memory of the attention layer.
+ *   "Untied Ulysses Pushes Llama-3-8B Training to 5 Million Tokens" (talk
+ *   write-up), paragraph on intermediate buffers: one group of heads is
+ *   computed, attention is run and a partial result is stored; the next group
+ *   reuses the buffers of the previous one; the attention formula itself is
+ *   unchanged.
+ *
+ * For chunk c (query heads cU .. cU+U-1 and the KV heads they read):
+ *   [Q_c|K_c|V_c] = x Wqkv[rows_c]^T, RoPE on Q_c and K_c,
+ *   O_c = causal_softmax(Q_c K_c^T / sqrt(d)) V_c   (plus LSE per head),
+ *   out32 += O_c Wo[:, cols_c]^T,                     out = bf16(out32).
+ * The backward pass recomputes Q_c/K_c/V_c (and O_c unless the caller kept
+ * it), and produces the chunk's dQ/dK/dV, its rows of dWqkv, its columns of
+ * dWo and its share of dx.  Every chunk reuses one workspace region, so the
+ * intermediate activation memory is proportional to U rather than H.
+ *
+ * Conventions (readings of points the pages leave open)
+ * -----------------------------------------------------
+ *  - Head dimension d = 128.  Query head h reads KV head h / g, g = H / Hkv.
+ *  - Causal mask: key j is visible to query i iff j <= i.  Scale 1/sqrt(d).
+ *  - RoPE pairs (i, i + d/2) of each head and rotates them by the angle
+ *    p * theta^(-2i/d) (p = token position, angle evaluated in fp64).
+ *  - Wqkv is [(H + 2 Hkv) d, D] row-major (rows: q heads, then k heads, then
+ *    v heads, d rows each); Wo is [D, H d] row-major (nn.Linear layout).
+ *  - LSE is the natural log of the row's sum of exp(scaled score), [H, L].
+ *  - Reductions are deterministic and do not depend on U: a run with any
+ *    valid U returns the same bits as a run with U = H.
+ *
+ * Memory, ownership, streams
+ * --------------------------
+ *  - Every pointer is a device pointer owned by the caller, including the
+ *    workspace `ws`, whose size comes from upipe_workspace_bytes().  The
+ *    library allocates no device memory.
+ *  - bf16 tensors are passed as `uint16_t*` holding bfloat16 bit patterns.
+ *  - Every pointer must be 16-byte aligned; tensors are dense row-major.
+ *  - Work is enqueued on `stream` (a cudaStream_t, 0 = legacy default) and
+ *    the call returns without waiting.  Calls that share a workspace must be
+ *    ordered on the GPU (for example, issued on one stream).
+ *
+ * Errors
+ * ------
+ * Every entry point returns 0 on success or a negative UPIPE_ERR_* code.
+ * Argument errors are detected on the host before anything is enqueued.
+ * Device-side waits are bounded (default 2 s, environment variable
+ * UPIPE_SPIN_LIMIT_NS overrides); a wait that runs out makes its kernel
+ * unwind and sets a device status word, read by upipe_last_device_status().
+ */
+#ifndef UPIPE_H_
+#define UPIPE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define UPIPE_OK 0
+#define UPIPE_ERR_INVALID_ARG (-1)        /* bad shape, null or misaligned pointer */
+#define UPIPE_ERR_WS_TOO_SMALL (-2)       /* ws_bytes < upipe_workspace_bytes(...) */
+#define UPIPE_ERR_CUDA (-3)               /* a CUDA runtime/driver call failed */
+#define UPIPE_ERR_DEVICE_TIMEOUT (-4)     /* a bounded device wait ran out */
+#define UPIPE_ERR_UNSUPPORTED_DEVICE (-5) /* current device is not sm_103 */
+
+/* Problem description.  All fields are read on every call.
+ *   L          tokens (1 .. 2^31-1)
+ *   D          hidden size; layer entries only, multiple of 128
+ *   H, Hkv     query / KV heads; H % Hkv == 0, H + 2*Hkv <= 96
+ *   d          head dimension; must be 128
+ *   U          query heads per chunk; H % U == 0 and (U % g == 0 or g % U == 0)
+ *   causal     must be 1
+ *   rope_theta RoPE base (> 0); layer entries only                          */
+typedef struct upipe_cfg {
+  int64_t L;
+  int32_t D;
+  int32_t H;
+  int32_t Hkv;
+  int32_t d;
+  int32_t U;
+  int32_t causal;
+  double rope_theta;
+} upipe_cfg;
+
+/* Workspace bytes for one call.
+ *   pass        0 = forward, 1 = backward
+ *   core_only   1 = upipe_attn_core_fwd / _bwd, 0 = the layer entries
+ *   has_o_saved 1 if the caller passes o_saved to the layer entries
+ * Returns 0 for an invalid configuration (or a call that needs none).      */
+size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved);
+
+/* Intermediate-activation accounting for one call (host arithmetic, no GPU):
+ *   chunk_bytes  workspace that scales with U: the chunk's Q/K/V/O buffers
+ *                and, in the backward pass, dO, Delta, dQ/dK/dV and the
+ *                dK/dV carry (U < g);
+ *   fixed_bytes  workspace that does not scale with U: the fp32 output carry
+ *                (out32 or dx32) and the RoPE table.
+ * Returns UPIPE_OK or UPIPE_ERR_INVALID_ARG.                                */
+int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved,
+                           size_t* chunk_bytes, size_t* fixed_bytes);
+
+/* Layer forward (the write-up's paragraph on intermediate buffers).
+ *   x        [L, D] bf16                 Wqkv [(H+2Hkv)*128, D] bf16
+ *   Wo       [D, H*128] bf16             out  [L, D] bf16 (written)
+ *   lse      [H, L] fp32 (written)
+ *   o_saved  [L, H*128] bf16 or NULL: when given, the attention output O is
+ *            written there (and may be passed to upipe_attn_bwd to skip the
+ *            recomputation of O); when NULL, O lives only in the workspace.
+ *   ws       workspace of at least upipe_workspace_bytes(cfg, 0, 0, o_saved != NULL) */
+int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                   uint16_t* out, float* lse, uint16_t* o_saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Layer backward: gradients of sum(out * dout).
+ *   dout     [L, D] bf16                 lse [H, L] fp32 from upipe_attn_fwd
+ *   o_saved  NULL (recompute O per chunk) or the tensor upipe_attn_fwd wrote
+ *   dx       [L, D] bf16 (written)
+ *   dWqkv    [(H+2Hkv)*128, D] fp32 (written, not accumulated)
+ *   dWo      [D, H*128] fp32 (written, not accumulated)
+ *   ws       workspace of at least upipe_workspace_bytes(cfg, 1, 0, o_saved != NULL) */
+int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                   const uint16_t* dout, const float* lse, const uint16_t* o_saved, uint16_t* dx, float* dWqkv,
+                   float* dWo, void* ws, size_t ws_bytes, void* stream);
+
+/* Attention core only (no projection, no RoPE), the per-rank slice that
+ * head-sharded context parallelism leaves on one GPU ("Untied Ulysses Pushes
+ * Llama-3-8B Training to 5 Million Tokens", paragraph on DeepSpeed Ulysses),
+ * processed U query heads at a time.
+ *   q, o     [L, H, 128] bf16            k, v [L, Hkv, 128] bf16
+ *   lse      [H, L] fp32 (written)       cfg->D and rope_theta are ignored.
+ *   ws       upipe_workspace_bytes(cfg, 0, 1, 0) bytes (0: may be NULL)      */
+int upipe_attn_core_fwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        uint16_t* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Core backward.  dout_o [L, H, 128] bf16 is the gradient of o; dq [L, H,
+ * 128], dk, dv [L, Hkv, 128] bf16 are written.                              */
+int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq, uint16_t* dk,
+                        uint16_t* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads and clears the device status word of
+ * the current device.  Returns UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT if a
+ * bounded wait of any earlier call ran out, or UPIPE_ERR_CUDA.              */
+int upipe_last_device_status(void* stream);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on
+ * an mbarrier nothing arrives on, with the given limit in nanoseconds, so
+ * that the wait runs out and sets the status word.  Returns a launch code. */
+int upipe_debug_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Launch accounting and per-kernel timing.
+ *   upipe_launch_count()  kernels this library has launched since load.
+ *   upipe_profile_enable(1) makes every later launch record a CUDA event
+ *   pair on the launching stream; upipe_profile_enable(0) stops recording.
+ *   upipe_profile_read() synchronizes on the recorded events, writes for
+ *   each kernel kind k < n its summed device time in ms (ms[k]) and launch
+ *   count (launches[k]), clears the record and returns the number of kinds
+ *   (UPIPE_KIND_COUNT).  Kinds are the UPIPE_KIND_* values below.          */
+#define UPIPE_KIND_ROPE_TABLE 0
+#define UPIPE_KIND_QKV_GEMM 1
+#define UPIPE_KIND_ATTN_FWD 2
+#define UPIPE_KIND_OPROJ_GEMM 3
+#define UPIPE_KIND_DO_GEMM 4
+#define UPIPE_KIND_DWO_GEMM 5
+#define UPIPE_KIND_ATTN_BWD_DQ 6
+#define UPIPE_KIND_ATTN_BWD_DKDV 7
+#define UPIPE_KIND_DWQKV_GEMM 8
+#define UPIPE_KIND_DX_GEMM 9
+#define UPIPE_KIND_DELTA 10
+#define UPIPE_KIND_COUNT 11
+int64_t upipe_launch_count(void);
+void upipe_profile_enable(int on);
+int upipe_profile_read(double* ms, int64_t* launches, int n);
+
+/* Static description of an error code. */
+const char* upipe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UPIPE_H_ */

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/upipe.h declares, plans workspaces by the stated
+arithmetic and rejects bad arguments before touching a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from headwise_chunked_context_gb300 import upipe
+from oracle import upipe_oracle as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "upipe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(upipe.LIB_PATH):
+        from headwise_chunked_context_gb300 import build
+        build.build()
+    return upipe.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(upipe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_uses():
+    assert declared_symbols() == sorted(upipe.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(upipe.strerror(code), str) and upipe.strerror(code)
+
+
+def _cfg(**kw):
+    base = dict(L=1024, D=1024, H=8, Hkv=2, U=2)
+    base.update(kw)
+    return upipe.Config(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(L=0), dict(H=6, Hkv=4), dict(U=3), dict(d=64), dict(causal=0), dict(D=1000),
+    dict(H=8, Hkv=2, U=8, D=0), dict(rope_theta=0.0), dict(H=8, Hkv=4, U=4, L=-5),
+    dict(H=96, Hkv=8, U=8),
+])
+def test_invalid_configs_have_no_workspace(lib, bad):
+    assert upipe.workspace_bytes(_cfg(**bad), 0) == 0
+    assert upipe.workspace_bytes(_cfg(**bad), 1) == 0
+
+
+def test_u_not_a_multiple_or_divisor_of_group_is_rejected(lib):
+    # H=12, Hkv=2 -> g=6; U=4 neither divides 6 nor is a multiple of it.
+    assert upipe.workspace_bytes(_cfg(H=12, Hkv=2, U=4), 0) == 0
+    assert upipe.workspace_bytes(_cfg(H=12, Hkv=2, U=3), 0) > 0
+    assert upipe.workspace_bytes(_cfg(H=12, Hkv=2, U=12), 0) > 0
+
+
+def test_entry_points_reject_bad_arguments_on_host(lib):
+    c = _cfg().c()
+    nullp = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: rejected first
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.upipe_attn_fwd(ctypes.byref(c), nullp, fake, fake, fake, fake, None, fake, 1 << 40, None) == -1
+    assert lib.upipe_attn_fwd(ctypes.byref(c), odd, fake, fake, fake, fake, None, fake, 1 << 40, None) == -1
+    assert lib.upipe_attn_fwd(ctypes.byref(c), fake, fake, fake, fake, fake, None, fake, 16, None) == -2
+    bad = _cfg(U=3).c()
+    assert lib.upipe_attn_bwd(ctypes.byref(bad), fake, fake, fake, fake, fake, None, fake, fake, fake, fake,
+                              1 << 40, None) == -1
+    assert lib.upipe_attn_core_bwd(ctypes.byref(c), fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                   0, None) == -2
+    assert lib.upipe_attn_core_fwd(None, fake, fake, fake, fake, fake, None, 0, None) == -1
+
+
+def test_workspace_arithmetic(lib):
+    L, D, H, Hkv, U = 1024, 1024, 8, 2, 2
+    c = _cfg()
+    slot = L * 128 * 2
+    al = lambda b: (b + 1023) // 1024 * 1024
+    kvc = 1
+    fwd = al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(L * D * 4)
+    assert upipe.workspace_bytes(c, 0) == fwd
+    assert upipe.workspace_bytes(c, 0, has_o_saved=True) == fwd - al(U * slot)
+    bwd = (al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(U * slot) + al(L * U * 4)
+           + al(2 * (U + 2 * kvc) * slot) + al(2 * L * 128 * 4) + al(L * D * 4))
+    assert upipe.workspace_bytes(c, 1) == bwd
+    # unchunked: no carries
+    assert upipe.workspace_bytes(_cfg(U=8), 0) == al(L * 64 * 8) + al(12 * slot) + al(8 * slot)
+    assert upipe.workspace_bytes(_cfg(), 0, core_only=True) == 0
+    assert upipe.workspace_bytes(_cfg(), 1, core_only=True) == al(L * U * 4) + al(2 * L * 128 * 4)
+
+
+@pytest.mark.parametrize("H,Hkv,L", [(32, 8, 32768), (64, 8, 131072), (32, 8, 65536)])
+def test_chunk_memory_scales_as_u_over_h(lib, H, Hkv, L):
+    D = 4096
+    full_f, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=H), 0)
+    full_b, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=H), 1)
+    g = H // Hkv
+    for U in [u for u in (g, 2 * g, H // 2) if H % u == 0 and u % g == 0]:
+        f, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=U), 0)
+        b, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=U), 1)
+        assert f * H == full_f * U
+        assert b * H == full_b * U
+        # the forward chunk buffers are exactly the oracle's Q/K/V/O arithmetic
+        assert f == orc.intermediate_bytes(L, U, H, Hkv, 128)
+
+
+def test_32b_shape_u8_saves_87_5_percent(lib):
+    L, D, H, Hkv = 131072, 5120, 64, 8
+    full, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=64), 1)
+    u8, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=8), 1)
+    assert 1 - u8 / full == pytest.approx(0.875, abs=0)

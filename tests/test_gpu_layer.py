@@ -1,0 +1,75 @@
+"""GPU parity of the whole head-chunked layer (projections, RoPE, causal
+attention, output projection; forward and backward) against the fp64
+oracle, through the C ABI, and bit-exactness of every chunk size against
+the unchunked run (U = H)."""
+
+import numpy as np
+import pytest
+import torch
+
+from headwise_chunked_context_gb300 import synth, upipe
+from oracle import upipe_oracle as orc
+from tests.gpu_common import dev, ensure_lib, f64, status_ok
+from tests.tolerance import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _run(shape, U, keep_o=False):
+    x, wqkv, wo, dout = synth.layer_inputs(shape)
+    cfg = upipe.Config(L=shape.L, D=shape.D, H=shape.H, Hkv=shape.Hkv, U=U, rope_theta=shape.theta)
+    xd, wd, wod, dd = dev(x, wqkv, wo, dout)
+    out, lse, o_saved = upipe.layer_forward(cfg, xd, wd, wod, keep_o=keep_o)
+    dx, dwqkv, dwo = upipe.layer_backward(cfg, xd, wd, wod, dd, lse, o_saved)
+    torch.cuda.synchronize()
+    status_ok()
+    return (x, wqkv, wo, dout), (out, lse, dx, dwqkv, dwo)
+
+
+def _check_vs_oracle(shape, inputs, outs):
+    x, wqkv, wo, dout = (f64(t) for t in inputs)
+    out, lse, dx, dwqkv, dwo = outs
+    rout, rlse, _ = orc.layer_fwd(x, wqkv, wo, shape.H, shape.Hkv, shape.theta)
+    assert_close(f64(out), rout, "out")
+    assert_close(f64(lse), rlse, "lse")
+    rdx, rdwqkv, rdwo = orc.layer_bwd(x, wqkv, wo, dout, shape.H, shape.Hkv, shape.theta)
+    assert_close(f64(dx), rdx, "dx")
+    assert_close(f64(dwqkv), rdwqkv, "dWqkv", weight_grad=True)
+    assert_close(f64(dwo), rdwo, "dWo", weight_grad=True)
+
+
+def test_tiny_config_matches_oracle():
+    """L=1024, D=1024, H=8, Hkv=2, U=2 (U < g), theta=500000."""
+    inputs, outs = _run(synth.TINY, synth.TINY.U)
+    _check_vs_oracle(synth.TINY, inputs, outs)
+
+
+@pytest.mark.parametrize("L,D,H,Hkv,U", [(200, 256, 4, 2, 2), (129, 128, 4, 1, 1), (384, 384, 8, 2, 4)])
+def test_ragged_layers_match_oracle(L, D, H, Hkv, U):
+    shape = synth.LayerShape(L=L, D=D, H=H, Hkv=Hkv, U=U)
+    inputs, outs = _run(shape, U)
+    _check_vs_oracle(shape, inputs, outs)
+
+
+@pytest.mark.parametrize("L,D,H,Hkv", [(1024, 1024, 8, 2), (333, 256, 8, 4)])
+def test_every_chunk_size_is_bit_exact_to_unchunked(L, D, H, Hkv):
+    shape = synth.LayerShape(L=L, D=D, H=H, Hkv=Hkv)
+    g = H // Hkv
+    _, ref = _run(shape, H)
+    for U in [u for u in range(1, H) if H % u == 0 and (u % g == 0 or g % u == 0)]:
+        _, outs = _run(shape, U)
+        for a, b, n in zip(ref, outs, ("out", "lse", "dx", "dWqkv", "dWo")):
+            assert torch.equal(a, b), f"U={U}: {n} differs from the unchunked run"
+
+
+def test_saved_o_matches_recompute():
+    shape = synth.LayerShape(L=300, D=256, H=4, Hkv=2)
+    _, a = _run(shape, 2, keep_o=False)
+    _, b = _run(shape, 2, keep_o=True)
+    for x, y, n in zip(a, b, ("out", "lse", "dx", "dWqkv", "dWo")):
+        assert torch.equal(x, y), n
