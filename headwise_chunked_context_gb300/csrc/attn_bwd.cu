@@ -11,56 +11,66 @@
 //
 // Two kernels, neither using atomics, so every result has one fixed fp32
 // summation order that does not depend on the chunk size U:
-//  * dq kernel: one CTA per (query head, 128-query tile) walks its KV blocks
-//    in ascending order and accumulates dQ in TMEM;
+//  * dq kernel: one CTA per (query head, 128-query tile) walks its 64-key
+//    blocks in ascending order and accumulates dQ in TMEM;
 //  * dkdv kernel: one CTA per (KV head, 128-key tile) walks the query heads
 //    that read this KV head (ascending) and, for each, the 64-query tiles at
 //    or after the key tile (ascending), accumulating dK and dV in TMEM.  When
 //    a chunk holds fewer query heads than a KV group (U < g) the partial sums
 //    are carried in fp32 between chunks and reloaded into TMEM, which keeps
 //    the same order as a single pass over the whole group.
+//
+// Both kernels: warp 8 loads tiles with TMA (the dkdv producer also copies
+// the query tile's LSE/Delta record), warp 9 issues tcgen05.mma, and warps 0-7
+// turn scores into P / dS: two warps share each TMEM lane quadrant and split
+// the columns, so every SM sub-partition has two of them to hide latency.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634074f;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // 8 compute warps, 1 producer warp, 1 MMA warp
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
-}
-
 // ============================================================== dQ kernel
+//
+// KV blocks of 64 keys stream through a 4-stage ring; the scores S and dP of
+// block j live in one of two TMEM buffers and dS in one of two shared tiles,
+// so the tensor core computes S/dP of block j+1 while the compute warps turn
+// block j into dS.
 
 namespace dq {
-constexpr int kTile = 128 * 128 * 2;
-constexpr int kHalf = kTile / 2;
+constexpr int kTileQ = 128 * 128 * 2;   // Q or dO: [128 queries][128 d]
+constexpr int kHalfQ = kTileQ / 2;
+constexpr int kTileK = 64 * 128 * 2;    // K or V block: [64 keys][128 d]
+constexpr int kHalfK = kTileK / 2;
+constexpr int kTileS = 128 * 64 * 2;    // dS: [128 queries][64 keys]
+constexpr int kStages = 4;              // K/V ring depth
 constexpr int OFF_Q = 0;
-constexpr int OFF_DO = OFF_Q + kTile;
-constexpr int OFF_K = OFF_DO + kTile;     // 2 stages
-constexpr int OFF_V = OFF_K + 2 * kTile;  // 2 stages
-constexpr int OFF_DS = OFF_V + 2 * kTile;
-constexpr int OFF_BAR = OFF_DS + kTile;
+constexpr int OFF_DO = OFF_Q + kTileQ;
+constexpr int OFF_KV = OFF_DO + kTileQ;  // per stage: K then V
+constexpr int OFF_DS = OFF_KV + kStages * 2 * kTileK;  // 2 buffers
+constexpr int OFF_BAR = OFF_DS + 2 * kTileS;
 enum {
   B_QDO_FULL,
-  B_K_FULL,
-  B_K_EMPTY = B_K_FULL + 2,
-  B_V_FULL = B_K_EMPTY + 2,
-  B_V_EMPTY = B_V_FULL + 2,
-  B_SDP_FULL = B_V_EMPTY + 2,
-  B_SDP_EMPTY,
-  B_DS_FULL,
-  B_DS_EMPTY,
-  B_DQ_DONE,
+  B_KV_FULL,
+  B_KV_EMPTY = B_KV_FULL + kStages,
+  B_SDP_FULL = B_KV_EMPTY + kStages,
+  B_SDP_EMPTY = B_SDP_FULL + 2,
+  B_DS_FULL = B_SDP_EMPTY + 2,
+  B_DS_EMPTY = B_DS_FULL + 2,
+  B_DQ_DONE = B_DS_EMPTY + 2,
   B_DRAIN,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
 constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
-constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;
+constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;  // S, dP: two 64-column buffers each
 }  // namespace dq
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -73,33 +83,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // most KV blocks first
   const int h = blockIdx.y;
   const int kz = p.k_z0 + h / p.g_loc;
   const int vz = p.v_z0 + h / p.g_loc;
-  const int n_kv = qb + 1;
+  const int n_kv = 2 * qb + 2;  // causal: 64-key blocks 0 .. 2 qb + 1
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QDO_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_K_FULL + s), 1);
-      mbar_init(bar(B_K_EMPTY + s), 1);
-      mbar_init(bar(B_V_FULL + s), 1);
-      mbar_init(bar(B_V_EMPTY + s), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_KV_FULL + s), 1);
+      mbar_init(bar(B_KV_EMPTY + s), 1);
     }
-    mbar_init(bar(B_SDP_FULL), 1);
-    mbar_init(bar(B_SDP_EMPTY), 4);
-    mbar_init(bar(B_DS_FULL), 4);
-    mbar_init(bar(B_DS_EMPTY), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SDP_FULL + b), 1);
+      mbar_init(bar(B_SDP_EMPTY + b), kComputeWarps);
+      mbar_init(bar(B_DS_FULL + b), kComputeWarps);
+      mbar_init(bar(B_DS_EMPTY + b), 1);
+    }
     mbar_init(bar(B_DQ_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sb + OFF_TMEM_SLOT, kTmemCols);
     tmem_relinquish();
   }
@@ -108,174 +118,187 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       tma_prefetch_map(&mq);
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
       tma_prefetch_map(&mdo);
-      mbar_expect_tx(bar(B_QDO_FULL), 2 * kTile);
+      mbar_expect_tx(bar(B_QDO_FULL), 2 * kTileQ);
       tma_load_3d(sb + OFF_Q, &mq, bar(B_QDO_FULL), 0, qb * 128, p.q_z0 + h);
-      tma_load_3d(sb + OFF_Q + kHalf, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
+      tma_load_3d(sb + OFF_Q + kHalfQ, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
       tma_load_3d(sb + OFF_DO, &mdo, bar(B_QDO_FULL), 0, qb * 128, p.do_z0 + h);
-      tma_load_3d(sb + OFF_DO + kHalf, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      tma_load_3d(sb + OFF_DO + kHalfQ, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
+      int last[kStages] = {-1, -1, -1, -1};
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(bar(B_K_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_K_FULL + s), kTile);
-        tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, j * 128, kz);
-        tma_load_3d(sb + OFF_K + s * kTile + kHalf, &mk, bar(B_K_FULL + s), 64, j * 128, kz);
-        last_k[s] = j;
-        if (!mbar_wait(bar(B_V_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_V_FULL + s), kTile);
-        tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, j * 128, vz);
-        tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, j * 128, vz);
-        last_v[s] = j;
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        if (!mbar_wait(bar(B_KV_EMPTY + s), ph ^ 1, w)) break;
+        const uint32_t ka = sb + OFF_KV + s * 2 * kTileK;
+        mbar_expect_tx(bar(B_KV_FULL + s), 2 * kTileK);
+        tma_load_3d(ka, &mk, bar(B_KV_FULL + s), 0, j * 64, kz);
+        tma_load_3d(ka + kHalfK, &mk, bar(B_KV_FULL + s), 64, j * 64, kz);
+        tma_load_3d(ka + kTileK, &mv, bar(B_KV_FULL + s), 0, j * 64, vz);
+        tma_load_3d(ka + kTileK + kHalfK, &mv, bar(B_KV_FULL + s), 64, j * 64, vz);
+        last[s] = j;
       }
       if (*abort_flag) {
         mbar_wait_drain(bar(B_QDO_FULL), 0, p.status);
-        for (int s = 0; s < 2; ++s) {
-          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] >> 1) & 1, p.status);
-          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] >> 1) & 1, p.status);
-        }
+        for (int s = 0; s < kStages; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar(B_KV_FULL + s), (last[s] / kStages) & 1, p.status);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
-      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dQ += dS K (K as MN-major B)
-      auto issue_dq = [&](int jj) -> bool {
-        const int s = jj & 1;
-        if (!mbar_wait(bar(B_DS_FULL), jj & 1, w)) return false;
-        tc_fence_after();
-        const uint32_t ka = sb + OFF_K + s * kTile;
+      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S = Q K^T, dP = dO V^T
+      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dQ += dS K (K as MN-major B)
+      // Event-driven issue: S/dP of block ns once its K/V stage has landed
+      // and the compute warps have read block ns - 2 out of the TMEM buffer;
+      // dQ += dS K of block nq once its dS tile is written.
+      auto sdp_ready = [&](int j) {
+        return mbar_try_wait(bar(B_KV_FULL + j % kStages), (j / kStages) & 1) &&
+               mbar_try_wait(bar(B_SDP_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
+      };
+      auto dq_ready = [&](int j) { return mbar_try_wait(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
+      auto issue_sdp = [&](int j) {
+        const int b = j & 1;
+        const uint32_t ka = sb + OFF_KV + (j % kStages) * 2 * kTileK;
+        const uint32_t va = ka + kTileK;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16(tmem + TM_DQ, sdesc_sw128(sb + OFF_DS + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                    sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_kn, (jj > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t qo = (kk >> 2) * kHalfQ + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
+          umma_bf16(tmem + TM_S + b * 64, sdesc_sw128(sb + OFF_Q + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
+                    id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_DS_EMPTY));
-        umma_commit(bar(B_K_EMPTY + s));
-        return true;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t qo = (kk >> 2) * kHalfQ + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
+          umma_bf16(tmem + TM_DP + b * 64, sdesc_sw128(sb + OFF_DO + qo, 16, 1024), sdesc_sw128(va + ko, 16, 1024),
+                    id_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_SDP_FULL + b));
+      };
+      auto issue_dq = [&](int j) {
+        const int b = j & 1;
+        const int st = j % kStages;
+        const uint32_t ka = sb + OFF_KV + st * 2 * kTileK;
+        const uint32_t da = sb + OFF_DS + b * kTileS;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16(tmem + TM_DQ, sdesc_sw128(da + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 2048, kHalfK, 1024),
+                    id_q, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_DS_EMPTY + b));
+        umma_commit(bar(B_KV_EMPTY + st));
       };
       bool ok = mbar_wait(bar(B_QDO_FULL), 0, w);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!(ok = mbar_wait(bar(B_K_FULL + s), ph, w))) break;
-        if (!(ok = mbar_wait(bar(B_V_FULL + s), ph, w))) break;
-        if (!(ok = mbar_wait(bar(B_SDP_EMPTY), (j & 1) ^ 1, w))) break;
-        tc_fence_after();
-        const uint32_t ka = sb + OFF_K + s * kTile;
-        const uint32_t va = sb + OFF_V + s * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_S, sdesc_sw128(sb + OFF_Q + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), id_kk,
-                    kk > 0 ? 1u : 0u);
+      int ns = 0, nq = 0;
+      Watchdog wd;
+      wd.reset();
+      while (ok && nq < n_kv) {
+        bool did = false;
+        if (ns < n_kv && sdp_ready(ns)) {
+          tc_fence_after();
+          issue_sdp(ns++);
+          did = true;
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_DP, sdesc_sw128(sb + OFF_DO + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), id_kk,
-                    kk > 0 ? 1u : 0u);
+        if (nq < ns && dq_ready(nq)) {
+          tc_fence_after();
+          issue_dq(nq++);
+          did = true;
         }
-        umma_commit(bar(B_SDP_FULL));
-        umma_commit(bar(B_V_EMPTY + s));
-        if (j >= 1) ok = issue_dq(j - 1);
+        if (did) wd.reset();
+        else ok = wd.alive(w);
       }
-      if (ok && issue_dq(n_kv - 1)) umma_commit(bar(B_DQ_DONE));
+      if (ok) umma_commit(bar(B_DQ_DONE));
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
   } else {
-    const int r = warp * 32 + lane;
+    // Compute warps: quadrant (warp & 3) of the TMEM lanes = query rows,
+    // half (warp >> 2) of the 64 key columns of each block.
+    const int quad = warp & 3;
+    const int half = warp >> 2;
+    const int r = quad * 32 + lane;
     const int qpos = qb * 128 + r;
     const bool valid = qpos < p.L;
-    const uint32_t trow = tmem_lane_addr(tmem, warp, 0);
+    const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
     const float sl2 = p.scale_log2;
-    const float lse2 = valid ? p.lse[static_cast<int64_t>(h) * p.L + qpos] * kLog2e : 0.f;
-    const float dlt = valid ? p.delta[static_cast<int64_t>(h) * p.L + qpos] : 0.f;
+    const int n_q64 = (p.L + 63) / 64;
+    const float* rec = p.ld + (static_cast<int64_t>(h) * n_q64 + (qpos >> 6)) * 128;
+    const float lse2 = valid ? rec[qpos & 63] : 0.f;
+    const float dlt = valid ? rec[64 + (qpos & 63)] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!(ok = warp_wait(bar(B_SDP_FULL), j & 1, w))) break;
-      if (!(ok = warp_wait(bar(B_DS_EMPTY), (j & 1) ^ 1, w))) break;
+      const int b = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!(ok = warp_wait(bar(B_SDP_FULL + b), ph, w))) break;
       tc_fence_after();
-      const bool diag = (j == qb);
+      uint32_t sv[32], dv[32];
+      tmem_ld32(trow + TM_S + b * 64 + half * 32, sv);
+      tmem_ld32(trow + TM_DP + b * 64 + half * 32, dv);
+      tmem_ld_wait(sv);
+      tmem_ld_wait(dv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY + b));
+      const int k0 = j * 64 + half * 32;  // key of this warp's first column
+      const bool near_diag = k0 + 31 > qpos;
+      uint32_t pk[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s0[32], s1[32], d0[32], d1[32];
-        tmem_ld32(trow + TM_S + half * 64, s0);
-        tmem_ld32(trow + TM_S + half * 64 + 32, s1);
-        tmem_ld32(trow + TM_DP + half * 64, d0);
-        tmem_ld32(trow + TM_DP + half * 64 + 32, d1);
-        tmem_ld_wait(s0);
-        tmem_ld_wait(s1);
-        tmem_ld_wait(d0);
-        tmem_ld_wait(d1);
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY));
+      for (int c = 0; c < 32; c += 2) {
+        float ds2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cc = c + e;
+          float pv = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -lse2));
+          if (near_diag && k0 + cc > qpos) pv = 0.f;
+          ds2[e] = pv * (__uint_as_float(dv[cc]) - dlt);
         }
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float ds2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            const float sv = __uint_as_float(cc < 32 ? s0[cc] : s1[cc - 32]);
-            const float dp = __uint_as_float(cc < 32 ? d0[cc] : d1[cc - 32]);
-            float pv = ex2_approx(fmaf(sv, sl2, -lse2));
-            if (diag && (half * 64 + cc) > r) pv = 0.f;
-            ds2[e] = pv * (dp - dlt);
-          }
-          pk[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
-        }
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(sb + OFF_DS + half * kHalf + sw128_offset(r, ch), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                       pk[4 * ch + 3]);
+        pk[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
       }
+      if (!(ok = warp_wait(bar(B_DS_EMPTY + b), ph ^ 1, w))) break;
+      const uint32_t da = sb + OFF_DS + b * kTileS;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        st_shared_v4(da + sw128_offset(r, half * 4 + ch), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                     pk[4 * ch + 3]);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DS_FULL));
+      if (lane == 0) mbar_arrive(bar(B_DS_FULL + b));
     }
     if (ok) ok = warp_wait(bar(B_DQ_DONE), 0, w);
     if (ok) {
+      // Epilogue: this warp writes RoPE pairs (i, i + 64), i in [32 half, 32 half + 32).
       tc_fence_after();
       __nv_bfloat16* out = p.dq + static_cast<int64_t>(qpos) * p.dq_row + static_cast<int64_t>(h) * p.dq_head;
       const float2* tab = p.rope ? p.rope + static_cast<int64_t>(qpos) * 64 : nullptr;
+      uint32_t a[32], b[32];
+      tmem_ld32(trow + TM_DQ + half * 32, a);
+      tmem_ld32(trow + TM_DQ + 64 + half * 32, b);
+      tmem_ld_wait(a);
+      tmem_ld_wait(b);
+      float lo[32], hi[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32], b[32];
-        tmem_ld32(trow + TM_DQ + half * 32, a);
-        tmem_ld32(trow + TM_DQ + 64 + half * 32, b);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b);
-        float lo[32], hi[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x0 = __uint_as_float(a[i]) * p.scale;
-          const float x1 = __uint_as_float(b[i]) * p.scale;
-          if (tab && valid) {
-            const float2 cs = tab[half * 32 + i];
-            lo[i] = x0 * cs.x + x1 * cs.y;
-            hi[i] = x1 * cs.x - x0 * cs.y;
-          } else {
-            lo[i] = x0;
-            hi[i] = x1;
-          }
+      for (int i = 0; i < 32; ++i) {
+        const float x0 = __uint_as_float(a[i]) * p.scale;
+        const float x1 = __uint_as_float(b[i]) * p.scale;
+        if (tab && valid) {
+          const float2 cs = tab[half * 32 + i];
+          lo[i] = x0 * cs.x + x1 * cs.y;
+          hi[i] = x1 * cs.x - x0 * cs.y;
+        } else {
+          lo[i] = x0;
+          hi[i] = x1;
         }
-        if (valid) {
+      }
+      if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            store8_bf16_split(out + half * 32 + q * 8, lo + 8 * q, p.lo_off);
-            store8_bf16_split(out + 64 + half * 32 + q * 8, hi + 8 * q, p.lo_off);
-          }
+        for (int q = 0; q < 4; ++q) {
+          store8_bf16_split(out + half * 32 + q * 8, lo + 8 * q, p.lo_off);
+          store8_bf16_split(out + 64 + half * 32 + q * 8, hi + 8 * q, p.lo_off);
         }
       }
     }
@@ -283,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -299,22 +322,22 @@ constexpr int kQHalf = kQ / 2;
 constexpr int kPT = 128 * 64 * 2;   // P^T or dS^T tile: [128 keys][64 queries]
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKV;
-constexpr int OFF_Q = OFF_V + kKV;     // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * kQ;  // 2 stages
-constexpr int OFF_PT = OFF_DO + 2 * kQ;  // 2 buffers
-constexpr int OFF_DST = OFF_PT + 2 * kPT;  // 2 buffers
-constexpr int OFF_LD = OFF_DST + 2 * kPT;  // 2 x (64 lse + 64 delta) floats
-constexpr int OFF_BAR = OFF_LD + 2 * 512;
+constexpr int kStages = 3;                 // Q/dO ring depth
+constexpr int OFF_Q = OFF_V + kKV;         // kStages stages
+constexpr int OFF_DO = OFF_Q + kStages * kQ;
+constexpr int OFF_PT = OFF_DO + kStages * kQ;  // 2 buffers
+constexpr int OFF_DST = OFF_PT + 2 * kPT;      // 2 buffers
+constexpr int OFF_LD = OFF_DST + 2 * kPT;      // per stage: the tile's LSE/Delta record
+constexpr int OFF_BAR = OFF_LD + kStages * 512;
 enum {
   B_KV_FULL,
   B_QDO_FULL,
-  B_QDO_EMPTY = B_QDO_FULL + 2,
-  B_SDP_FULL = B_QDO_EMPTY + 2,
+  B_QDO_EMPTY = B_QDO_FULL + kStages,
+  B_SDP_FULL = B_QDO_EMPTY + kStages,
   B_SDP_EMPTY = B_SDP_FULL + 2,
   B_PDS_FULL = B_SDP_EMPTY + 2,
   B_PDS_EMPTY = B_PDS_FULL + 2,
-  B_LD_READY = B_PDS_EMPTY + 2,
-  B_CARRY_READY = B_LD_READY + 2,
+  B_CARRY_READY = B_PDS_EMPTY + 2,
   B_DKV_DONE,
   B_DRAIN,
   B_COUNT
@@ -335,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kb = gridDim.x - 1 - blockIdx.x;  // key tiles near the start see the most queries
+  const int kb = blockIdx.x;  // key tile 0 sees every query: the heaviest tiles launch first
   const int kv = blockIdx.y;
   const int n_q64 = (p.L + 63) / 64;
   const int nqi = n_q64 - 2 * kb;  // query tiles at or after this key tile
@@ -344,25 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
   const bool carry_in = p.carry_in != 0;
+  float* ld_smem = reinterpret_cast<float*>(smem + OFF_LD);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_QDO_FULL + s), 1);
       mbar_init(bar(B_QDO_EMPTY + s), 1);
-      mbar_init(bar(B_SDP_FULL + s), 1);
-      mbar_init(bar(B_SDP_EMPTY + s), 4);
-      mbar_init(bar(B_PDS_FULL + s), 4);
-      mbar_init(bar(B_PDS_EMPTY + s), 1);
-      mbar_init(bar(B_LD_READY + s), 128);
     }
-    mbar_init(bar(B_CARRY_READY), 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_SDP_FULL + s), 1);
+      mbar_init(bar(B_SDP_EMPTY + s), kComputeWarps);
+      mbar_init(bar(B_PDS_FULL + s), kComputeWarps);
+      mbar_init(bar(B_PDS_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_CARRY_READY), kComputeWarps);
     mbar_init(bar(B_DKV_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sb + OFF_TMEM_SLOT, kTmemCols);
     tmem_relinquish();
   }
@@ -371,8 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
+    // Q and dO tiles (TMA) plus the tile's LSE/Delta record (bulk copy), all
+    // on one barrier per stage.
     if (lane == 0) {
+      int last[kStages] = {-1, -1, -1};
       tma_prefetch_map(&mq);
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
@@ -382,63 +410,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sb + OFF_K + kKVHalf, &mk, bar(B_KV_FULL), 64, kb * 128, p.k_z0 + kv);
       tma_load_3d(sb + OFF_V, &mv, bar(B_KV_FULL), 0, kb * 128, p.v_z0 + kv);
       tma_load_3d(sb + OFF_V + kKVHalf, &mv, bar(B_KV_FULL), 64, kb * 128, p.v_z0 + kv);
-      int last[2] = {-1, -1};
       for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
         const int hl = kv * p.g_loc + it / nqi;
         const int qi = 2 * kb + it % nqi;
         if (!mbar_wait(bar(B_QDO_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kQ);
+        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kQ + 512);
         tma_load_3d(sb + OFF_Q + s * kQ, &mq, bar(B_QDO_FULL + s), 0, qi * 64, p.q_z0 + hl);
         tma_load_3d(sb + OFF_Q + s * kQ + kQHalf, &mq, bar(B_QDO_FULL + s), 64, qi * 64, p.q_z0 + hl);
         tma_load_3d(sb + OFF_DO + s * kQ, &mdo, bar(B_QDO_FULL + s), 0, qi * 64, p.do_z0 + hl);
         tma_load_3d(sb + OFF_DO + s * kQ + kQHalf, &mdo, bar(B_QDO_FULL + s), 64, qi * 64, p.do_z0 + hl);
+        bulk_load(sb + OFF_LD + s * 512, p.ld + (static_cast<int64_t>(hl) * n_q64 + qi) * 128, 512,
+                  bar(B_QDO_FULL + s));
         last[s] = it;
       }
       if (*abort_flag) {
         mbar_wait_drain(bar(B_KV_FULL), 0, p.status);
-        for (int s = 0; s < 2; ++s)
-          if (last[s] >= 0) mbar_wait_drain(bar(B_QDO_FULL + s), (last[s] >> 1) & 1, p.status);
+        for (int s = 0; s < kStages; ++s)
+          if (last[s] >= 0) mbar_wait_drain(bar(B_QDO_FULL + s), (last[s] / kStages) & 1, p.status);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
       constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // dV += P^T dO, dK += dS^T Q
-      auto issue_grad = [&](int ii) -> bool {
-        const int s = ii & 1;
-        const uint32_t ph = (ii >> 1) & 1;
-        if (!mbar_wait(bar(B_PDS_FULL + s), ph, w)) return false;
-        tc_fence_after();
-        const uint32_t pt = sb + OFF_PT + s * kPT;
-        const uint32_t dst = sb + OFF_DST + s * kPT;
-        const uint32_t qa = sb + OFF_Q + s * kQ;
-        const uint32_t da = sb + OFF_DO + s * kQ;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + TM_DV, sdesc_sw128(pt + kk * 32, 16, 1024), sdesc_sw128(da + kk * 2048, kQHalf, 1024),
-                    id_g, (carry_in || ii > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + TM_DK, sdesc_sw128(dst + kk * 32, 16, 1024), sdesc_sw128(qa + kk * 2048, kQHalf, 1024),
-                    id_g, (carry_in || ii > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_PDS_EMPTY + s));
-        umma_commit(bar(B_QDO_EMPTY + s));
-        return true;
+      // Event-driven issue: S^T/dP^T of tile ns once its Q/dO stage has
+      // landed and the compute warps have read tile ns - 2 out of the TMEM
+      // buffer; dV/dK products of tile ng once its P^T/dS^T tiles are written.
+      auto sdp_ready = [&](int it) {
+        return mbar_try_wait(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1) &&
+               mbar_try_wait(bar(B_SDP_EMPTY + (it & 1)), ((it >> 1) & 1) ^ 1);
       };
-      bool ok = mbar_wait(bar(B_KV_FULL), 0, w);
-      if (ok && carry_in) ok = mbar_wait(bar(B_CARRY_READY), 0, w);
-      for (int it = 0; ok && it < n_it; ++it) {
+      auto grad_ready = [&](int it) { return mbar_try_wait(bar(B_PDS_FULL + (it & 1)), (it >> 1) & 1); };
+      auto issue_sdp = [&](int it) {
         const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        if (!(ok = mbar_wait(bar(B_QDO_FULL + s), ph, w))) break;
-        if (!(ok = mbar_wait(bar(B_SDP_EMPTY + s), ph ^ 1, w))) break;
-        tc_fence_after();
-        const uint32_t qa = sb + OFF_Q + s * kQ;
-        const uint32_t da = sb + OFF_DO + s * kQ;
+        const int qs = it % kStages;
+        const uint32_t qa = sb + OFF_Q + qs * kQ;
+        const uint32_t da = sb + OFF_DO + qs * kQ;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
@@ -454,105 +463,135 @@ __global__ void __launch_bounds__(kThreads, 1)
                     id_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(B_SDP_FULL + s));
-        if (it >= 1) ok = issue_grad(it - 1);
+      };
+      auto issue_grad = [&](int it) {
+        const int s = it & 1;
+        const int qs = it % kStages;
+        const uint32_t pt = sb + OFF_PT + s * kPT;
+        const uint32_t dst = sb + OFF_DST + s * kPT;
+        const uint32_t qa = sb + OFF_Q + qs * kQ;
+        const uint32_t da = sb + OFF_DO + qs * kQ;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16(tmem + TM_DV, sdesc_sw128(pt + kk * 32, 16, 1024), sdesc_sw128(da + kk * 2048, kQHalf, 1024),
+                    id_g, (carry_in || it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16(tmem + TM_DK, sdesc_sw128(dst + kk * 32, 16, 1024), sdesc_sw128(qa + kk * 2048, kQHalf, 1024),
+                    id_g, (carry_in || it > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_PDS_EMPTY + s));
+        umma_commit(bar(B_QDO_EMPTY + qs));
+      };
+      bool ok = mbar_wait(bar(B_KV_FULL), 0, w);
+      if (ok && carry_in) ok = mbar_wait(bar(B_CARRY_READY), 0, w);
+      int ns = 0, ng = 0;
+      Watchdog wd;
+      wd.reset();
+      while (ok && ng < n_it) {
+        bool did = false;
+        if (ns < n_it && sdp_ready(ns)) {
+          tc_fence_after();
+          issue_sdp(ns++);
+          did = true;
+        }
+        if (ng < ns && grad_ready(ng)) {
+          tc_fence_after();
+          issue_grad(ng++);
+          did = true;
+        }
+        if (did) wd.reset();
+        else ok = wd.alive(w);
       }
-      if (ok && issue_grad(n_it - 1)) umma_commit(bar(B_DKV_DONE));
+      if (ok) umma_commit(bar(B_DKV_DONE));
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
   } else {
-    const int r = warp * 32 + lane;  // key row = TMEM lane
+    // Compute warps: quadrant (warp & 3) of the key rows, half (warp >> 2) of
+    // the 64 query columns of each tile.
+    const int quad = warp & 3;
+    const int half = warp >> 2;
+    const int r = quad * 32 + lane;  // key row = TMEM lane
     const int kpos = kb * 128 + r;
     const bool valid = kpos < p.L;
-    const uint32_t trow = tmem_lane_addr(tmem, warp, 0);
+    const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
     const float sl2 = p.scale_log2;
-    float* carry_k = p.dkv_carry + (static_cast<int64_t>(kv * 2 + 0) * p.L + kpos) * kHeadDim;
-    float* carry_v = p.dkv_carry + (static_cast<int64_t>(kv * 2 + 1) * p.L + kpos) * kHeadDim;
+    // Warps 0-3 own dK, warps 4-7 own dV (carry load and epilogue).
+    float* my_carry =
+        p.dkv_carry + (static_cast<int64_t>(kv * 2 + half) * p.L + kpos) * kHeadDim;
+    const int my_col = half == 0 ? TM_DK : TM_DV;
     bool ok = true;
     if (carry_in) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float* src = t == 0 ? carry_k : carry_v;
-        const int col = t == 0 ? TM_DK : TM_DV;
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 x = valid ? ld_global_nc_v4(src + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-          }
-          tmem_st32(trow + col + c4 * 32, v);
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x = valid ? ld_global_nc_v4(my_carry + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
+          v[4 * q] = x.x;
+          v[4 * q + 1] = x.y;
+          v[4 * q + 2] = x.z;
+          v[4 * q + 3] = x.w;
         }
+        tmem_st32(trow + my_col + c4 * 32, v);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_CARRY_READY));
     }
-    float* ld_smem = reinterpret_cast<float*>(smem + OFF_LD);
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      const int hl = kv * p.g_loc + it / nqi;
       const int qi = 2 * kb + it % nqi;
-      {  // this query tile's LSE (log2 domain) and Delta into shared memory
-        const int c = threadIdx.x & 63;
-        const int q = qi * 64 + c;
-        float val;
-        if (threadIdx.x < 64)
-          val = q < p.L ? p.lse[static_cast<int64_t>(hl) * p.L + q] * kLog2e : INFINITY;
-        else
-          val = q < p.L ? p.delta[static_cast<int64_t>(hl) * p.L + q] : 0.f;
-        ld_smem[s * 128 + threadIdx.x] = val;
-        mbar_arrive(bar(B_LD_READY + s));
-      }
-      if (!(ok = warp_wait(bar(B_LD_READY + s), ph, w))) break;
       if (!(ok = warp_wait(bar(B_SDP_FULL + s), ph, w))) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32], d0[32], d1[32];
-      tmem_ld32(trow + TM_ST + s * 64, s0);
-      tmem_ld32(trow + TM_ST + s * 64 + 32, s1);
-      tmem_ld32(trow + TM_DPT + s * 64, d0);
-      tmem_ld32(trow + TM_DPT + s * 64 + 32, d1);
-      tmem_ld_wait(s0);
-      tmem_ld_wait(s1);
-      tmem_ld_wait(d0);
-      tmem_ld_wait(d1);
+      uint32_t sv[32], dv[32];
+      tmem_ld32(trow + TM_ST + s * 64 + half * 32, sv);
+      tmem_ld32(trow + TM_DPT + s * 64 + half * 32, dv);
+      tmem_ld_wait(sv);
+      tmem_ld_wait(dv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY + s));
-
-      const float* lse_s = ld_smem + s * 128;
-      const float* dl_s = lse_s + 64;
-      const bool near_diag = qi * 64 < kb * 128 + 128;
-      uint32_t pp[32], dd[32];
+      const int qs = it % kStages;
+      if (!(ok = warp_wait(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
+      const float4* l4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + half * 32);
+      const float4* d4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + 64 + half * 32);
+      const int q0 = qi * 64 + half * 32;
+      const bool near_diag = q0 < kpos;  // some of this warp's queries precede this key
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float pv2[2], ds2[2];
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 lv = l4[c4];
+        const float4 dl = d4[c4];
+        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+        const float da[4] = {dl.x, dl.y, dl.z, dl.w};
+        float pv[4], ds[4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          const float sv = __uint_as_float(cc < 32 ? s0[cc] : s1[cc - 32]);
-          const float dp = __uint_as_float(cc < 32 ? d0[cc] : d1[cc - 32]);
-          float pv = ex2_approx(fmaf(sv, sl2, -lse_s[cc]));
-          if (near_diag && qi * 64 + cc < kpos) pv = 0.f;
-          pv2[e] = pv;
-          ds2[e] = pv * (dp - dl_s[cc]);
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c4 * 4 + e;
+          float pr = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -la[e]));
+          if (near_diag && q0 + cc < kpos) pr = 0.f;
+          pv[e] = pr;
+          ds[e] = pr * (__uint_as_float(dv[cc]) - da[e]);
         }
-        pp[c >> 1] = pack_bf16x2(pv2[0], pv2[1]);
-        dd[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
+        pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+        pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        dd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
       if (!(ok = warp_wait(bar(B_PDS_EMPTY + s), ph ^ 1, w))) break;
       const uint32_t pt = sb + OFF_PT + s * kPT;
       const uint32_t dst = sb + OFF_DST + s * kPT;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        st_shared_v4(pt + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2], pp[4 * ch + 3]);
-        st_shared_v4(dst + sw128_offset(r, ch), dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
+      for (int ch = 0; ch < 4; ++ch) {
+        st_shared_v4(pt + sw128_offset(r, half * 4 + ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
+                     pp[4 * ch + 3]);
+        st_shared_v4(dst + sw128_offset(r, half * 4 + ch), dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
+                     dd[4 * ch + 3]);
       }
       fence_async_smem();
       __syncwarp();
@@ -563,31 +602,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (p.carry_out) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float* dstp = t == 0 ? carry_k : carry_v;
-          const int col = t == 0 ? TM_DK : TM_DV;
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(trow + my_col + c4 * 32, v);
+          tmem_ld_wait(v);
+          if (valid) {
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t v[32];
-            tmem_ld32(trow + col + c4 * 32, v);
-            tmem_ld_wait(v);
-            if (valid) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                st_global_v4(dstp + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int q = 0; q < 8; ++q)
+              st_global_v4(my_carry + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
-      } else {
-        // dK: scale, rotate back by -angle (layer path), bf16.
+      } else if (half == 0) {
+        // dK: scale, rotate back by -angle (layer path), bf16 (+ residual).
         __nv_bfloat16* outk = p.dk + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head;
-        __nv_bfloat16* outv = p.dv + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head;
         const float2* tab = p.rope ? p.rope + static_cast<int64_t>(kpos) * 64 : nullptr;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t a[32], b[32];
-          tmem_ld32(trow + TM_DK + half * 32, a);
-          tmem_ld32(trow + TM_DK + 64 + half * 32, b);
+          tmem_ld32(trow + TM_DK + hh * 32, a);
+          tmem_ld32(trow + TM_DK + 64 + hh * 32, b);
           tmem_ld_wait(a);
           tmem_ld_wait(b);
           float lo[32], hi[32];
@@ -596,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float x0 = __uint_as_float(a[i]) * p.scale;
             const float x1 = __uint_as_float(b[i]) * p.scale;
             if (tab && valid) {
-              const float2 cs = tab[half * 32 + i];
+              const float2 cs = tab[hh * 32 + i];
               lo[i] = x0 * cs.x + x1 * cs.y;
               hi[i] = x1 * cs.x - x0 * cs.y;
             } else {
@@ -607,11 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              store8_bf16_split(outk + half * 32 + q * 8, lo + 8 * q, p.lo_off);
-              store8_bf16_split(outk + 64 + half * 32 + q * 8, hi + 8 * q, p.lo_off);
+              store8_bf16_split(outk + hh * 32 + q * 8, lo + 8 * q, p.lo_off);
+              store8_bf16_split(outk + 64 + hh * 32 + q * 8, hi + 8 * q, p.lo_off);
             }
           }
         }
+      } else {
+        __nv_bfloat16* outv = p.dv + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t v[32];
@@ -631,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -639,13 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k64, const CUtensorMap& v64,
                                const CUtensorMap& dO, const AttnBwdParams& p, int n_qblocks, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(n_qblocks, p.nheads);
-  attn_bwd_dq_kernel<<<grid, kThreads, dq::kSmemBytes, s>>>(q, k, v, dO, p);
+  attn_bwd_dq_kernel<<<grid, kThreads, dq::kSmemBytes, s>>>(q, k64, v64, dO, p);
   return cudaGetLastError();
 }
 

@@ -43,8 +43,7 @@ enum {
   B_S_EMPTY = B_S_FULL + 2,
   B_P_FULL = B_S_EMPTY + 2,
   B_P_EMPTY = B_P_FULL + 2,
-  B_PV_DONE = B_P_EMPTY + 2,
-  B_DRAIN,
+  B_DRAIN = B_P_EMPTY + 2,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
@@ -55,10 +54,6 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int TM_S = 0;    // two score buffers: columns [0,128) and [128,256)
 constexpr int TM_O = 256;  // O accumulator: [256, 384)
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -89,7 +84,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_P_FULL + s), 4);
       mbar_init(bar(B_P_EMPTY + s), 1);
     }
-    mbar_init(bar(B_PV_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -140,33 +134,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
       constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj & 1;
-        const uint32_t ph = (jj >> 1) & 1;
-        if (!mbar_wait(bar(B_P_FULL + s), ph, w)) return false;
-        if (!mbar_wait(bar(B_V_FULL + s), ph, w)) return false;
-        tc_fence_after();
-        const uint32_t pa = sb + OFF_P + s * kTile;
-        const uint32_t va = sb + OFF_V + s * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(va + kk * 2048, kHalf, 1024);
-          umma_bf16(tmem + TM_O, a, b, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_P_EMPTY + s));
-        umma_commit(bar(B_V_EMPTY + s));
-        umma_commit(bar(B_PV_DONE));
-        return true;
+      // Event-driven issue: every pass issues S(ns) once K(ns) has landed and
+      // the softmax warps have read S(ns - 2) out of its TMEM buffer, and
+      // O += P(np) V(np) once P(np) is in shared memory, so the tensor core
+      // never idles behind a wait that another queued product could fill.
+      auto s_ready = [&](int j) {
+        return mbar_try_wait(bar(B_K_FULL + (j & 1)), (j >> 1) & 1) &&
+               mbar_try_wait(bar(B_S_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
       };
-      bool ok = mbar_wait(bar(B_Q_FULL), 0, w);
-      tc_fence_after();
-      for (int j = 0; ok && j < n_kv; ++j) {
+      auto pv_ready = [&](int j) {
+        return mbar_try_wait(bar(B_P_FULL + (j & 1)), (j >> 1) & 1) &&
+               mbar_try_wait(bar(B_V_FULL + (j & 1)), (j >> 1) & 1);
+      };
+      auto issue_s = [&](int j) {
         const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!(ok = mbar_wait(bar(B_K_FULL + s), ph, w))) break;
-        if (!(ok = mbar_wait(bar(B_S_EMPTY + s), ph ^ 1, w))) break;
-        tc_fence_after();
         const uint32_t ka = sb + OFF_K + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -176,9 +157,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(bar(B_S_FULL + s));
         umma_commit(bar(B_K_EMPTY + s));
-        if (j >= 1) ok = issue_pv(j - 1);
+      };
+      auto issue_pv = [&](int j) {
+        const int s = j & 1;
+        const uint32_t pa = sb + OFF_P + s * kTile;
+        const uint32_t va = sb + OFF_V + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(va + kk * 2048, kHalf, 1024);
+          umma_bf16(tmem + TM_O, a, b, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_P_EMPTY + s));
+        umma_commit(bar(B_V_EMPTY + s));
+      };
+      bool ok = mbar_wait(bar(B_Q_FULL), 0, w);
+      int ns = 0, np = 0;
+      Watchdog wd;
+      wd.reset();
+      while (ok && np < n_kv) {
+        bool did = false;
+        if (ns < n_kv && s_ready(ns)) {
+          tc_fence_after();
+          issue_s(ns++);
+          did = true;
+        }
+        if (np < ns && pv_ready(np)) {
+          tc_fence_after();
+          issue_pv(np++);
+          did = true;
+        }
+        if (did) wd.reset();
+        else ok = wd.alive(w);
       }
-      if (ok) issue_pv(n_kv - 1);
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
@@ -228,8 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m_use, mx * sl2);
       const bool need = m_new > m_use + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds PV(0..j-1): wait for PV(j-1), then rescale the rows that moved.
-        if (!(ok = warp_wait(bar(B_PV_DONE), (j - 1) & 1, w))) break;
+        // O holds PV(0..j-1): wait for PV(j-1) (it releases P buffer (j-1) & 1),
+        // then rescale the rows that moved.
+        if (!(ok = warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, w))) break;
         tc_fence_after();
         const float f = need ? ex2_approx(m_use - m_new) : 1.f;
 #pragma unroll
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL + s));
     }
-    if (ok) ok = warp_wait(bar(B_PV_DONE), (n_kv - 1) & 1, w);
+    if (ok) ok = warp_wait(bar(B_P_EMPTY + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, w);
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;

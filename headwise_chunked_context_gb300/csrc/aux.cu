@@ -32,19 +32,24 @@ __global__ void rope_table_kernel(float2* __restrict__ table, int64_t L, const _
   table[idx] = make_float2(c, s);
 }
 
-// Delta[h][p] = sum_k dO[p, h, k] * O[p, h, k] for the core backward entry.
+// LSE/Delta records for the core backward entry: for head h and row p,
+// Delta = sum_k dO[p, h, k] * O[p, h, k] and LSE * log2(e), stored per
+// 64-row tile as [64 LSE*log2(e) | 64 Delta]; rows past L get +inf / 0.
 // 16 lanes per (row, head): each lane reads 16 bytes of O and of dO.
 __global__ void delta_kernel(const __nv_bfloat16* __restrict__ o, int64_t o_row, int64_t o_head,
                              const __nv_bfloat16* __restrict__ dO, int64_t do_row, int64_t do_head,
-                             float* __restrict__ delta, int64_t L, int nheads) {
+                             const float* __restrict__ lse, float* __restrict__ ld, int64_t L, int nheads) {
+  const int64_t n_q64 = (L + 63) / 64;
+  const int64_t rows = n_q64 * 64;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t item = gid >> 4;  // (head, row)
   const int sub = threadIdx.x & 15;
-  const bool live = item < L * nheads;
-  const int64_t hh = live ? item / L : 0;
-  const int64_t row = live ? item % L : 0;
+  const bool live = item < rows * nheads;
+  const int64_t hh = live ? item / rows : 0;
+  const int64_t row = live ? item % rows : 0;
+  const bool in = live && row < L;
   float acc = 0.f;
-  if (live) {
+  if (in) {
     const uint4 a = ld_global_nc_v4(o + row * o_row + hh * o_head + sub * 8);
     const uint4 b = ld_global_nc_v4(dO + row * do_row + hh * do_head + sub * 8);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w};
@@ -57,7 +62,11 @@ __global__ void delta_kernel(const __nv_bfloat16* __restrict__ o, int64_t o_row,
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (live && sub == 0) delta[hh * L + row] = acc;
+  if (live && sub == 0) {
+    float* rec = ld + (hh * n_q64 + (row >> 6)) * 128;
+    rec[row & 63] = in ? lse[hh * L + row] * 1.4426950408889634074f : INFINITY;
+    rec[64 + (row & 63)] = in ? acc : 0.f;
+  }
 }
 
 // One thread waits on an mbarrier that nothing arrives on.  The bounded wait
@@ -90,12 +99,13 @@ cudaError_t launch_rope_table(float2* table, int64_t L, double theta, cudaStream
 }
 
 cudaError_t launch_delta(const __nv_bfloat16* o, int64_t o_row, int64_t o_head, const __nv_bfloat16* dO,
-                         int64_t do_row, int64_t do_head, float* delta, int64_t L, int nheads, cudaStream_t s) {
-  const int64_t threads_total = L * nheads * 16;
+                         int64_t do_row, int64_t do_head, const float* lse, float* ld, int64_t L, int nheads,
+                         cudaStream_t s) {
+  const int64_t threads_total = (L + 63) / 64 * 64 * nheads * 16;
   const int threads = 256;
   const int64_t blocks = (threads_total + threads - 1) / threads;
-  delta_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(o, o_row, o_head, dO, do_row, do_head, delta, L,
-                                                                  nheads);
+  delta_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(o, o_row, o_head, dO, do_row, do_head, lse, ld,
+                                                                  L, nheads);
   return cudaGetLastError();
 }
 

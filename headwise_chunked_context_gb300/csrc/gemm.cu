@@ -106,10 +106,6 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
   else return sdesc_sw128(base + kk * 32, 16, 1024);
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
@@ -311,7 +307,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           }
         }
-        if (valid) p.delta[static_cast<int64_t>(slot) * p.L + m] = dsum;
+        // LSE/Delta record of this row (padding rows past L get +inf / 0).
+        const int n_q64 = (p.L + 63) / 64;
+        if (m < n_q64 * 64) {
+          float* rec = p.ld_rec + (static_cast<int64_t>(slot) * n_q64 + (m >> 6)) * 128;
+          rec[m & 63] = valid ? p.lse_in[static_cast<int64_t>(slot) * p.L + m] * 1.4426950408889634074f : INFINITY;
+          rec[64 + (m & 63)] = valid ? dsum : 0.f;
+        }
       } else {
         // fp32 or carried outputs: OPROJ, DX (carry / final bf16), DWO, DWQKV (fp32).
         float* frow = nullptr;

@@ -103,6 +103,36 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
+// Warp-wide wait: lane 0 polls (bounded), the outcome is broadcast, then
+// every lane observes the completed phase once itself (its own acquire), so
+// that only one lane per warp spins on the barrier word.  Must be called by
+// all 32 lanes; the result is warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try_wait(bar, parity);
+  return ok != 0;
+}
+
+// No-progress watchdog for a thread that polls several barriers with
+// non-blocking try_wait and issues whatever is ready: `alive` turns false
+// (raising the abort flag and the timeout status) once `limit_ns` passes
+// without progress, or as soon as another thread of the CTA aborted.
+struct Watchdog {
+  uint64_t t0;
+  __device__ __forceinline__ void reset() { t0 = global_timer_ns(); }
+  __device__ __forceinline__ bool alive(const WaitCtl& w) {
+    if (*w.abort_flag) return false;
+    if (global_timer_ns() - t0 > w.limit_ns) {
+      *w.abort_flag = 1;
+      atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
+      return false;
+    }
+    return true;
+  }
+};
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
@@ -124,6 +154,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst),
       "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -70,6 +70,12 @@ struct Plan {
   size_t fixed_bytes() const { return carry32 + rope; }
 };
 
+// LSE/Delta records of the backward: per head of the chunk and 64-query
+// tile, 64 LSE*log2(e) then 64 Delta floats.
+size_t ld_records_bytes(const Shape& s) {
+  return static_cast<size_t>(s.U) * static_cast<size_t>((s.L + 63) / 64) * 128 * sizeof(float);
+}
+
 Plan make_plan(const Shape& s, int pass, bool core, bool o_saved) {
   Plan p;
   const size_t L = static_cast<size_t>(s.L);
@@ -77,7 +83,7 @@ Plan make_plan(const Shape& s, int pass, bool core, bool o_saved) {
   const bool carry_kv = s.U < s.g;       // dK/dV carried across the chunks of a group
   if (core) {
     if (pass == 1) {
-      p.delta = L * s.U * 4;
+      p.delta = ld_records_bytes(s);
       if (carry_kv) p.dkv_carry = 2 * L * kHeadDim * 4;
     }
   } else {
@@ -87,7 +93,7 @@ Plan make_plan(const Shape& s, int pass, bool core, bool o_saved) {
     if (s.nch > 1) p.carry32 = L * s.D * 4;
     if (pass == 1) {
       p.dO = s.U * slot;
-      p.delta = L * s.U * 4;
+      p.delta = ld_records_bytes(s);
       p.dqkv = 2 * (s.U + 2 * s.kvc) * slot;  // high then low bf16 halves
       if (carry_kv) p.dkv_carry = 2 * L * kHeadDim * 4;
     }
@@ -479,7 +485,8 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     d.out = dO;
     d.o_rows = obuf + o_col0;
     d.ld_o = ld_o;
-    d.delta = delta;
+    d.lse_in = lse + static_cast<int64_t>(ch.q0) * L;
+    d.ld_rec = delta;
     UPIPE_LAUNCH(UPIPE_KIND_DO_GEMM, launch_gemm(GK_DO, m_dout, m_wo_mn, d, st));
 
     // dWo[:, cols_c] = dout^T O_c.
@@ -507,8 +514,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     b.k_z0 = s.U;
     b.v_z0 = s.U + s.kvc;
     b.do_z0 = 0;
-    b.lse = lse + static_cast<int64_t>(ch.q0) * L;
-    b.delta = delta;
+    b.ld = delta;
     b.scale = scale;
     b.scale_log2 = scale_log2;
     b.dq = dqkv;
@@ -525,7 +531,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     b.rope = rope;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv64, m_qkv64, m_do, b, m_tiles, st));
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(m_qkv64, m_qkv, m_qkv, m_do64, b, m_tiles, st));
 
     // dWqkv rows of the chunk: q slots always, k/v slots once complete.
@@ -647,11 +653,13 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
   const int64_t L = s.L;
   const int m_tiles = static_cast<int>((L + 127) / 128);
   const int64_t Hd = static_cast<int64_t>(s.H) * 128, Hkvd = static_cast<int64_t>(s.Hkv) * 128;
-  CUtensorMap mq, mq64, mk, mv, mdo, mdo64;
+  CUtensorMap mq, mq64, mk, mv, mk64, mv64, mdo, mdo64;
   UPIPE_MAP(map3d(&mq, q, L, s.H, Hd, 128, 128));
   UPIPE_MAP(map3d(&mq64, q, L, s.H, Hd, 128, 64));
   UPIPE_MAP(map3d(&mk, k, L, s.Hkv, Hkvd, 128, 128));
   UPIPE_MAP(map3d(&mv, v, L, s.Hkv, Hkvd, 128, 128));
+  UPIPE_MAP(map3d(&mk64, k, L, s.Hkv, Hkvd, 128, 64));
+  UPIPE_MAP(map3d(&mv64, v, L, s.Hkv, Hkvd, 128, 64));
   UPIPE_MAP(map3d(&mdo, dout_o, L, s.H, Hd, 128, 128));
   UPIPE_MAP(map3d(&mdo64, dout_o, L, s.H, Hd, 128, 64));
   const int chunks_per_group = s.U < s.g ? s.g / s.U : 1;
@@ -659,8 +667,8 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     const Chunk ch = chunk_of(s, c);
     const int cg = c % chunks_per_group;
     UPIPE_LAUNCH(UPIPE_KIND_DELTA, launch_delta(reinterpret_cast<const bf16*>(o) + static_cast<int64_t>(ch.q0) * 128, Hd, 128,
-                          reinterpret_cast<const bf16*>(dout_o) + static_cast<int64_t>(ch.q0) * 128, Hd, 128, delta,
-                          L, s.U, st));
+                          reinterpret_cast<const bf16*>(dout_o) + static_cast<int64_t>(ch.q0) * 128, Hd, 128,
+                          lse + static_cast<int64_t>(ch.q0) * L, delta, L, s.U, st));
     AttnBwdParams b;
     std::memset(&b, 0, sizeof(b));
     b.L = static_cast<int>(L);
@@ -671,8 +679,7 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.k_z0 = ch.kv0;
     b.v_z0 = ch.kv0;
     b.do_z0 = ch.q0;
-    b.lse = lse + static_cast<int64_t>(ch.q0) * L;
-    b.delta = delta;
+    b.ld = delta;
     b.scale = static_cast<float>(1.0 / std::sqrt(128.0));
     b.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
     b.dq = reinterpret_cast<bf16*>(dq) + static_cast<int64_t>(ch.q0) * 128;
@@ -688,7 +695,7 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.rope = nullptr;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk, mv, mdo, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk64, mv64, mdo, b, m_tiles, st));
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(mq64, mk, mv, mdo64, b, m_tiles, st));
   }
   return UPIPE_OK;

@@ -49,7 +49,8 @@ struct GemmParams {
   const float2* rope;          // [L, 64] (cos, sin)
   const __nv_bfloat16* o_rows; // DO: O_c rows for Delta
   int64_t ld_o;
-  float* delta;                // DO: [U, L]
+  const float* lse_in;         // DO: the chunk's LSE rows [U, L]
+  float* ld_rec;               // DO: per 64-query tile records (see AttnBwdParams::ld)
   int lo_z;                    // DWQKV / DX: A slot offset of the low bf16 halves (0 = no split)
   int* status;
   uint64_t limit_ns;
@@ -79,8 +80,10 @@ struct AttnBwdParams {
   int g_loc;    // query heads per KV head in this launch
   int nkv;      // KV heads in this launch
   int q_z0, k_z0, v_z0, do_z0;
-  const float* lse;    // [nheads, L]
-  const float* delta;  // [nheads, L]
+  // Per local head h and 64-query tile t, a 128-float record at
+  // ld + (h * ceil(L/64) + t) * 128: LSE * log2(e) of the tile's 64 queries
+  // (+inf past L), then their Delta = rowsum(dO * O) (0 past L).
+  const float* ld;
   float scale;         // 1/sqrt(d)
   float scale_log2;    // log2(e)/sqrt(d)
   __nv_bfloat16* dq;   // dQ of local head h, row p: dq + p*dq_row + h*dq_head
@@ -103,13 +106,16 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& 
                         cudaStream_t s);
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const AttnFwdParams& p, int n_qblocks, cudaStream_t s);
-cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+// q, dO: 128-row boxes; k64, v64: 64-row boxes.
+cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k64, const CUtensorMap& v64,
                                const CUtensorMap& dO, const AttnBwdParams& p, int n_qblocks, cudaStream_t s);
 cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dO64, const AttnBwdParams& p, int n_kblocks, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int64_t L, double theta, cudaStream_t s);
+// Writes the LSE/Delta records of AttnBwdParams::ld for `nheads` heads.
 cudaError_t launch_delta(const __nv_bfloat16* o, int64_t o_row, int64_t o_head, const __nv_bfloat16* dO,
-                         int64_t do_row, int64_t do_head, float* delta, int64_t L, int nheads, cudaStream_t s);
+                         int64_t do_row, int64_t do_head, const float* lse, float* ld, int64_t L, int nheads,
+                         cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace upipe

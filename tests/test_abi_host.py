@@ -91,13 +91,14 @@ def test_workspace_arithmetic(lib):
     fwd = al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(L * D * 4)
     assert upipe.workspace_bytes(c, 0) == fwd
     assert upipe.workspace_bytes(c, 0, has_o_saved=True) == fwd - al(U * slot)
-    bwd = (al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(U * slot) + al(L * U * 4)
+    rec = U * ((L + 63) // 64) * 128 * 4  # LSE/Delta records
+    bwd = (al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(U * slot) + al(rec)
            + al(2 * (U + 2 * kvc) * slot) + al(2 * L * 128 * 4) + al(L * D * 4))
     assert upipe.workspace_bytes(c, 1) == bwd
     # unchunked: no carries
     assert upipe.workspace_bytes(_cfg(U=8), 0) == al(L * 64 * 8) + al(12 * slot) + al(8 * slot)
     assert upipe.workspace_bytes(_cfg(), 0, core_only=True) == 0
-    assert upipe.workspace_bytes(_cfg(), 1, core_only=True) == al(L * U * 4) + al(2 * L * 128 * 4)
+    assert upipe.workspace_bytes(_cfg(), 1, core_only=True) == al(rec) + al(2 * L * 128 * 4)
 
 
 @pytest.mark.parametrize("H,Hkv,L", [(32, 8, 32768), (64, 8, 131072), (32, 8, 65536)])
