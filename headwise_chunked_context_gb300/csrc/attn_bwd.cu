@@ -36,6 +36,53 @@ constexpr int kMmaWarp = 9;
 constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
+// dS row slice of the dq kernel: 32 keys of one query row.  kMask applies
+// the causal mask (only the two 64-key blocks of the diagonal tile need it).
+template <bool kMask>
+__device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float sl2, float lse2,
+                                         float dlt, int k0, int qpos, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float ds2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int cc = c + e;
+      float pv = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -lse2));
+      if (kMask && k0 + cc > qpos) pv = 0.f;
+      ds2[e] = pv * (__uint_as_float(dv[cc]) - dlt);
+    }
+    pk[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
+  }
+}
+
+// P^T and dS^T row slice of the dkdv kernel: 32 queries of one key row.
+// kMask zeroes queries before the key (only the first two query tiles).
+template <bool kMask>
+__device__ __forceinline__ void pds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* l4,
+                                          const float4* d4, float sl2, int q0, int kpos, uint32_t (&pp)[16],
+                                          uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const float4 lv = l4[c4];
+    const float4 dl = d4[c4];
+    const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+    const float da[4] = {dl.x, dl.y, dl.z, dl.w};
+    float pv[4], ds[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int cc = c4 * 4 + e;
+      float pr = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -la[e]));
+      if (kMask && q0 + cc < kpos) pr = 0.f;
+      pv[e] = pr;
+      ds[e] = pr * (__uint_as_float(dv[cc]) - da[e]);
+    }
+    pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+    pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+    dd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+    dd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+  }
+}
+
 // ============================================================== dQ kernel
 //
 // KV blocks of 64 keys stream through a 4-stage ring; the scores S and dP of
@@ -156,10 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and the compute warps have read block ns - 2 out of the TMEM buffer;
       // dQ += dS K of block nq once its dS tile is written.
       auto sdp_ready = [&](int j) {
-        return mbar_try_wait(bar(B_KV_FULL + j % kStages), (j / kStages) & 1) &&
-               mbar_try_wait(bar(B_SDP_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
+        return mbar_test(bar(B_KV_FULL + j % kStages), (j / kStages) & 1) &&
+               mbar_test(bar(B_SDP_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
       };
-      auto dq_ready = [&](int j) { return mbar_try_wait(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
+      auto dq_ready = [&](int j) { return mbar_test(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
       auto issue_sdp = [&](int j) {
         const int b = j & 1;
         const uint32_t ka = sb + OFF_KV + (j % kStages) * 2 * kTileK;
@@ -245,20 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY + b));
       const int k0 = j * 64 + half * 32;  // key of this warp's first column
-      const bool near_diag = k0 + 31 > qpos;
       uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float ds2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          float pv = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -lse2));
-          if (near_diag && k0 + cc > qpos) pv = 0.f;
-          ds2[e] = pv * (__uint_as_float(dv[cc]) - dlt);
-        }
-        pk[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
-      }
+      if (j >= 2 * qb)  // the diagonal tile (warp-uniform)
+        ds_slice<true>(sv, dv, sl2, lse2, dlt, k0, qpos, pk);
+      else
+        ds_slice<false>(sv, dv, sl2, lse2, dlt, k0, qpos, pk);
       if (!(ok = warp_wait(bar(B_DS_EMPTY + b), ph ^ 1, w))) break;
       const uint32_t da = sb + OFF_DS + b * kTileS;
 #pragma unroll
@@ -439,10 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // landed and the compute warps have read tile ns - 2 out of the TMEM
       // buffer; dV/dK products of tile ng once its P^T/dS^T tiles are written.
       auto sdp_ready = [&](int it) {
-        return mbar_try_wait(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1) &&
-               mbar_try_wait(bar(B_SDP_EMPTY + (it & 1)), ((it >> 1) & 1) ^ 1);
+        return mbar_test(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1) &&
+               mbar_test(bar(B_SDP_EMPTY + (it & 1)), ((it >> 1) & 1) ^ 1);
       };
-      auto grad_ready = [&](int it) { return mbar_try_wait(bar(B_PDS_FULL + (it & 1)), (it >> 1) & 1); };
+      auto grad_ready = [&](int it) { return mbar_test(bar(B_PDS_FULL + (it & 1)), (it >> 1) & 1); };
       auto issue_sdp = [&](int it) {
         const int s = it & 1;
         const int qs = it % kStages;
@@ -561,28 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* l4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + half * 32);
       const float4* d4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + 64 + half * 32);
       const int q0 = qi * 64 + half * 32;
-      const bool near_diag = q0 < kpos;  // some of this warp's queries precede this key
       uint32_t pp[16], dd[16];
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 lv = l4[c4];
-        const float4 dl = d4[c4];
-        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-        const float da[4] = {dl.x, dl.y, dl.z, dl.w};
-        float pv[4], ds[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c4 * 4 + e;
-          float pr = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -la[e]));
-          if (near_diag && q0 + cc < kpos) pr = 0.f;
-          pv[e] = pr;
-          ds[e] = pr * (__uint_as_float(dv[cc]) - da[e]);
-        }
-        pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-        pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-        dd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-        dd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-      }
+      if (qi < 2 * kb + 2)  // query tiles overlapping the key tile (warp-uniform)
+        pds_slice<true>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
+      else
+        pds_slice<false>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
       if (!(ok = warp_wait(bar(B_PDS_EMPTY + s), ph ^ 1, w))) break;
       const uint32_t pt = sb + OFF_PT + s * kPT;
       const uint32_t dst = sb + OFF_DST + s * kPT;

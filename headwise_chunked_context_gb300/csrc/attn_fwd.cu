@@ -139,12 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O += P(np) V(np) once P(np) is in shared memory, so the tensor core
       // never idles behind a wait that another queued product could fill.
       auto s_ready = [&](int j) {
-        return mbar_try_wait(bar(B_K_FULL + (j & 1)), (j >> 1) & 1) &&
-               mbar_try_wait(bar(B_S_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
+        return mbar_test(bar(B_K_FULL + (j & 1)), (j >> 1) & 1) &&
+               mbar_test(bar(B_S_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
       };
       auto pv_ready = [&](int j) {
-        return mbar_try_wait(bar(B_P_FULL + (j & 1)), (j >> 1) & 1) &&
-               mbar_try_wait(bar(B_V_FULL + (j & 1)), (j >> 1) & 1);
+        return mbar_test(bar(B_P_FULL + (j & 1)), (j >> 1) & 1) &&
+               mbar_test(bar(B_V_FULL + (j & 1)), (j >> 1) & 1);
       };
       auto issue_s = [&](int j) {
         const int s = j & 1;

@@ -64,6 +64,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: true iff the phase of parity `parity` has completed.
+// (try_wait may suspend the thread for a while; a thread that polls several
+// barriers and issues whichever is ready must not block on any one of them.)
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA wait control: the shared abort flag, the device status word and
 // the time limit of one wait.
 struct WaitCtl {
