@@ -7,19 +7,21 @@
 // Llama-3-8B Training to 5 Million Tokens", paragraph on intermediate
 // buffers: "not a new attention formula, but a different memory schedule").
 //
-// Design (sm_103a):
-//  * one CTA = one 128-query tile of one head; CTAs are launched heaviest
-//    (most KV blocks) first so the causal triangle balances across SMs;
-//  * warp 4 streams Q once and K/V blocks of 128 keys through a two-stage
-//    TMA ring (128-byte swizzle);
-//  * warp 5 issues tcgen05.mma from one thread: S = Q K^T into one of two
-//    TMEM score buffers while the softmax warps work on the other, then
-//    O += P V into a TMEM accumulator;
-//  * warps 0-3 own one query row per thread (the TMEM lane), so the row max
-//    and row sum are thread-local.  They write P as bf16 into a swizzled
-//    shared tile (the A operand of the P V product).  O is rescaled in TMEM
-//    only when a row maximum grows by more than 2^8, which keeps every
-//    exponent bounded and the result exact up to rounding.
+// Design (sm_103a).  The tensor core reads shared-memory operands at about
+// 128 B/clk per SM, which an M=128 product with both operands in shared
+// memory saturates; so everything that can live in TMEM does:
+//  * one CTA = one 128-query tile of one head, heaviest (most KV blocks)
+//    first so the causal triangle balances across SMs;
+//  * warp 4 streams Q once and K/V blocks of 128 keys through 3-stage TMA
+//    rings (128-byte swizzle); the softmax warps copy Q into TMEM once;
+//  * warp 5 issues tcgen05.mma from one thread, event-driven: S(j) = Q K^T
+//    with Q from TMEM into one of two TMEM score buffers, and O += P V with
+//    P read from TMEM;
+//  * warps 0-3 own one query row per thread (the TMEM lane), so row max and
+//    row sum are thread-local; they write P as packed bf16 back over the
+//    scores they just read.  O is rescaled in TMEM only when a row maximum
+//    grows by more than 2^8, which bounds every exponent and keeps the
+//    result exact up to rounding.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -27,22 +29,22 @@ namespace {
 
 constexpr int kTile = 128 * 128 * 2;  // [128][128] bf16, stored as two 64-column halves
 constexpr int kHalf = kTile / 2;
+constexpr int kStages = 3;            // K and V ring depth
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + kTile;      // 2 stages
-constexpr int OFF_V = OFF_K + 2 * kTile;  // 2 stages
-constexpr int OFF_P = OFF_V + 2 * kTile;  // 2 buffers
-constexpr int OFF_BAR = OFF_P + 2 * kTile;
+constexpr int OFF_K = OFF_Q + kTile;
+constexpr int OFF_V = OFF_K + kStages * kTile;
+constexpr int OFF_BAR = OFF_V + kStages * kTile;
 
 enum {
   B_Q_FULL,
-  B_K_FULL,     // +2
-  B_K_EMPTY = B_K_FULL + 2,
-  B_V_FULL = B_K_EMPTY + 2,
-  B_V_EMPTY = B_V_FULL + 2,
-  B_S_FULL = B_V_EMPTY + 2,
-  B_S_EMPTY = B_S_FULL + 2,
-  B_P_FULL = B_S_EMPTY + 2,
-  B_P_EMPTY = B_P_FULL + 2,
+  B_Q_TMEM,  // Q copied into TMEM by the softmax warps
+  B_K_FULL,
+  B_K_EMPTY = B_K_FULL + kStages,
+  B_V_FULL = B_K_EMPTY + kStages,
+  B_V_EMPTY = B_V_FULL + kStages,
+  B_S_FULL = B_V_EMPTY + kStages,
+  B_P_FULL = B_S_FULL + 2,
+  B_P_EMPTY = B_P_FULL + 2,  // P V of that buffer done: buffer free, O up to date
   B_DRAIN = B_P_EMPTY + 2,
   B_COUNT
 };
@@ -52,8 +54,9 @@ constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;  // + alignment slack
 
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int TM_S = 0;    // two score buffers: columns [0,128) and [128,256)
-constexpr int TM_O = 256;  // O accumulator: [256, 384)
+constexpr int TM_Q = 0;    // Q, packed bf16: columns [0, 64)
+constexpr int TM_S = 64;   // two score buffers of 128 columns; P(j) overwrites the first 64 of its own
+constexpr int TM_O = 320;  // O accumulator: [320, 448)
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -74,15 +77,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(bar(B_Q_TMEM), 4);
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_K_FULL + s), 1);
       mbar_init(bar(B_K_EMPTY + s), 1);
       mbar_init(bar(B_V_FULL + s), 1);
       mbar_init(bar(B_V_EMPTY + s), 1);
-      mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_EMPTY + s), 4);
-      mbar_init(bar(B_P_FULL + s), 4);
-      mbar_init(bar(B_P_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_S_FULL + b), 1);
+      mbar_init(bar(B_P_FULL + b), 4);
+      mbar_init(bar(B_P_EMPTY + b), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -106,10 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(bar(B_Q_FULL), kTile);
       tma_load_3d(sb + OFF_Q, &mq, bar(B_Q_FULL), 0, qb * 128, p.q_z0 + h);
       tma_load_3d(sb + OFF_Q + kHalf, &mq, bar(B_Q_FULL), 64, qb * 128, p.q_z0 + h);
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      int last_k[kStages], last_v[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_k[s] = last_v[s] = -1;
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
         if (!mbar_wait(bar(B_K_EMPTY + s), ph ^ 1, w)) break;
         mbar_expect_tx(bar(B_K_FULL + s), kTile);
         tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, j * 128, kz);
@@ -123,55 +130,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {  // let every issued copy land before the CTA exits
         mbar_wait_drain(bar(B_Q_FULL), 0, p.status);
-        for (int s = 0; s < 2; ++s) {
-          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] >> 1) & 1, p.status);
-          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] >> 1) & 1, p.status);
+        for (int s = 0; s < kStages; ++s) {
+          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] / kStages) & 1, p.status);
+          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] / kStages) & 1, p.status);
         }
       }
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (K-major) x V (MN-major)
-      // Event-driven issue: every pass issues S(ns) once K(ns) has landed and
-      // the softmax warps have read S(ns - 2) out of its TMEM buffer, and
-      // O += P(np) V(np) once P(np) is in shared memory, so the tensor core
-      // never idles behind a wait that another queued product could fill.
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q (TMEM) x K (smem, K-major)
+      constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (TMEM) x V (smem, MN-major)
+      // Event-driven issue: S(ns) once K(ns) has landed and P V of block
+      // ns - 2 (whose P occupies the same TMEM buffer) has completed; P V of
+      // block np once the softmax warps have written P(np).
       auto s_ready = [&](int j) {
-        return mbar_test(bar(B_K_FULL + (j & 1)), (j >> 1) & 1) &&
-               mbar_test(bar(B_S_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
+        return mbar_test(bar(B_K_FULL + j % kStages), (j / kStages) & 1) &&
+               mbar_test(bar(B_P_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
       };
       auto pv_ready = [&](int j) {
         return mbar_test(bar(B_P_FULL + (j & 1)), (j >> 1) & 1) &&
-               mbar_test(bar(B_V_FULL + (j & 1)), (j >> 1) & 1);
+               mbar_test(bar(B_V_FULL + j % kStages), (j / kStages) & 1);
       };
       auto issue_s = [&](int j) {
-        const int s = j & 1;
+        const int b = j & 1;
+        const int s = j % kStages;
         const uint32_t ka = sb + OFF_K + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_S + s * 128, sdesc_sw128(sb + OFF_Q + off, 16, 1024),
-                    sdesc_sw128(ka + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + TM_S + b * 128, tmem + TM_Q + kk * 8,
+                       sdesc_sw128(ka + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_S_FULL + s));
+        umma_commit(bar(B_S_FULL + b));
         umma_commit(bar(B_K_EMPTY + s));
       };
       auto issue_pv = [&](int j) {
-        const int s = j & 1;
-        const uint32_t pa = sb + OFF_P + s * kTile;
+        const int b = j & 1;
+        const int s = j % kStages;
         const uint32_t va = sb + OFF_V + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = sdesc_sw128(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(va + kk * 2048, kHalf, 1024);
-          umma_bf16(tmem + TM_O, a, b, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + TM_O, tmem + TM_S + b * 128 + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_o,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_P_EMPTY + s));
+        umma_commit(bar(B_P_EMPTY + b));
         umma_commit(bar(B_V_EMPTY + s));
       };
-      bool ok = mbar_wait(bar(B_Q_FULL), 0, w);
+      bool ok = mbar_wait(bar(B_Q_TMEM), 0, w);
+      tc_fence_after();
       int ns = 0, np = 0;
       Watchdog wd;
       wd.reset();
@@ -201,24 +207,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_use = -INFINITY;  // running max used as the exponent offset (log2 domain)
     float l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j & 1;
+    // Q row r -> TMEM (packed bf16, element pairs per column).
+    bool ok = warp_wait(bar(B_Q_FULL), 0, w);
+    if (ok) {
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t q[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = ld_shared_v4(sb + OFF_Q + hq * kHalf + sw128_offset(r, ch));
+          q[4 * ch] = v.x;
+          q[4 * ch + 1] = v.y;
+          q[4 * ch + 2] = v.z;
+          q[4 * ch + 3] = v.w;
+        }
+        tmem_st32(trow + TM_Q + hq * 32, q);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_Q_TMEM));
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!(ok = warp_wait(bar(B_S_FULL + s), ph, w))) break;
+      if (!(ok = warp_wait(bar(B_S_FULL + b), ph, w))) break;
       tc_fence_after();
+      const uint32_t tsb = trow + TM_S + b * 128;
       uint32_t v0[32], v1[32], v2[32], v3[32];
-      tmem_ld32(trow + TM_S + s * 128 + 0, v0);
-      tmem_ld32(trow + TM_S + s * 128 + 32, v1);
-      tmem_ld32(trow + TM_S + s * 128 + 64, v2);
-      tmem_ld32(trow + TM_S + s * 128 + 96, v3);
+      tmem_ld32(tsb + 0, v0);
+      tmem_ld32(tsb + 32, v1);
+      tmem_ld32(tsb + 64, v2);
+      tmem_ld32(tsb + 96, v3);
       tmem_ld_wait(v0);
       tmem_ld_wait(v1);
       tmem_ld_wait(v2);
       tmem_ld_wait(v3);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + s));
 
       float x[128];
 #pragma unroll
@@ -239,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m_use, mx * sl2);
       const bool need = m_new > m_use + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds PV(0..j-1): wait for PV(j-1) (it releases P buffer (j-1) & 1),
+        // O holds PV(0..j-1): wait for PV(j-1) (it releases buffer (j-1) & 1),
         // then rescale the rows that moved.
         if (!(ok = warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, w))) break;
         tc_fence_after();
@@ -253,33 +277,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
           tmem_st32(trow + TM_O + c4 * 32, o);
         }
-        tmem_st_wait();
         l *= f;
       }
       if (need) m_use = m_new;
 
-      uint32_t pk[64];
+      uint32_t pk0[32], pk1[32];
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
+      for (int c = 0; c < 64; c += 2) {
         const float p0 = ex2_approx(fmaf(x[c], sl2, -m_use));
         const float p1 = ex2_approx(fmaf(x[c + 1], sl2, -m_use));
-        rs += p0 + p1;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
+        const float p2 = ex2_approx(fmaf(x[64 + c], sl2, -m_use));
+        const float p3 = ex2_approx(fmaf(x[64 + c + 1], sl2, -m_use));
+        rs += (p0 + p1) + (p2 + p3);
+        pk0[c >> 1] = pack_bf16x2(p0, p1);
+        pk1[c >> 1] = pack_bf16x2(p2, p3);
       }
       l += rs;
-
-      if (!(ok = warp_wait(bar(B_P_EMPTY + s), ph ^ 1, w))) break;
-      const uint32_t pa = sb + OFF_P + s * kTile;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        st_shared_v4(pa + (ch >> 3) * kHalf + sw128_offset(r, ch & 7), pk[4 * ch], pk[4 * ch + 1],
-                     pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_async_smem();
+      // P over the scores just read (columns [0, 64) of this buffer).
+      tmem_st32(tsb + 0, pk0);
+      tmem_st32(tsb + 32, pk1);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL + s));
+      if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
     }
     if (ok) ok = warp_wait(bar(B_P_EMPTY + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, w);
     if (ok) {
