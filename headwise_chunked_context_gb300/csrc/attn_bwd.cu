@@ -36,50 +36,60 @@ constexpr int kMmaWarp = 9;
 constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
-// dS row slice of the dq kernel: 32 keys of one query row.  kMask applies
-// the causal mask (only the two 64-key blocks of the diagonal tile need it).
+// dS row slice of the dq kernel: 32 keys of one query row, paired fp32
+// math.  kMask applies the causal mask (only the diagonal tile needs it).
 template <bool kMask>
-__device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float sl2, float lse2,
+__device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float sl2, float nlse2,
                                          float dlt, int k0, int qpos, uint32_t (&pk)[16]) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const uint64_t nlx2 = f2_pack(nlse2, nlse2);
+  const uint64_t dlx2 = f2_pack(dlt, dlt);
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
-    float ds2[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int cc = c + e;
-      float pv = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -lse2));
-      if (kMask && k0 + cc > qpos) pv = 0.f;
-      ds2[e] = pv * (__uint_as_float(dv[cc]) - dlt);
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nlx2), t0, t1);
+    float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+    if (kMask) {
+      if (k0 + c > qpos) p0 = 0.f;
+      if (k0 + c + 1 > qpos) p1 = 0.f;
     }
-    pk[c >> 1] = pack_bf16x2(ds2[0], ds2[1]);
+    const uint64_t d = f2_sub(f2_pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), dlx2);
+    float d0, d1;
+    f2_unpack(f2_mul(f2_pack(p0, p1), d), d0, d1);
+    pk[c >> 1] = pack_bf16x2(d0, d1);
   }
 }
 
-// P^T and dS^T row slice of the dkdv kernel: 32 queries of one key row.
-// kMask zeroes queries before the key (only the first two query tiles).
+// P^T and dS^T row slice of the dkdv kernel: 32 queries of one key row,
+// paired fp32 math.  kMask zeroes queries before the key (first two tiles).
 template <bool kMask>
 __device__ __forceinline__ void pds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* l4,
                                           const float4* d4, float sl2, int q0, int kpos, uint32_t (&pp)[16],
                                           uint32_t (&dd)[16]) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
   for (int c4 = 0; c4 < 8; ++c4) {
-    const float4 lv = l4[c4];
-    const float4 dl = d4[c4];
-    const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-    const float da[4] = {dl.x, dl.y, dl.z, dl.w};
-    float pv[4], ds[4];
+    const float4 lv = l4[c4];  // -LSE * log2(e)
+    const float4 dl = d4[c4];  // Delta
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4; e += 2) {
       const int cc = c4 * 4 + e;
-      float pr = ex2_approx(fmaf(__uint_as_float(sv[cc]), sl2, -la[e]));
-      if (kMask && q0 + cc < kpos) pr = 0.f;
-      pv[e] = pr;
-      ds[e] = pr * (__uint_as_float(dv[cc]) - da[e]);
+      const float la0 = e == 0 ? lv.x : lv.z, la1 = e == 0 ? lv.y : lv.w;
+      const float da0 = e == 0 ? dl.x : dl.z, da1 = e == 0 ? dl.y : dl.w;
+      float t0, t1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[cc]), __uint_as_float(sv[cc + 1])), sl2x2, f2_pack(la0, la1)), t0,
+                t1);
+      float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+      if (kMask) {
+        if (q0 + cc < kpos) p0 = 0.f;
+        if (q0 + cc + 1 < kpos) p1 = 0.f;
+      }
+      const uint64_t d = f2_sub(f2_pack(__uint_as_float(dv[cc]), __uint_as_float(dv[cc + 1])), f2_pack(da0, da1));
+      float s0, s1;
+      f2_unpack(f2_mul(f2_pack(p0, p1), d), s0, s1);
+      pp[cc >> 1] = pack_bf16x2(p0, p1);
+      dd[cc >> 1] = pack_bf16x2(s0, s1);
     }
-    pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-    pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-    dd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-    dd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
   }
 }
 
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const int n_q64 = (p.L + 63) / 64;
     const float* rec = p.ld + (static_cast<int64_t>(h) * n_q64 + (qpos >> 6)) * 128;
-    const float lse2 = valid ? rec[qpos & 63] : 0.f;
+    const float nlse2 = valid ? rec[qpos & 63] : 0.f;  // -LSE * log2(e)
     const float dlt = valid ? rec[64 + (qpos & 63)] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -294,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = j * 64 + half * 32;  // key of this warp's first column
       uint32_t pk[16];
       if (j >= 2 * qb)  // the diagonal tile (warp-uniform)
-        ds_slice<true>(sv, dv, sl2, lse2, dlt, k0, qpos, pk);
+        ds_slice<true>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
       else
-        ds_slice<false>(sv, dv, sl2, lse2, dlt, k0, qpos, pk);
+        ds_slice<false>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
       if (!(ok = warp_wait(bar(B_DS_EMPTY + b), ph ^ 1, w))) break;
       const uint32_t da = sb + OFF_DS + b * kTileS;
 #pragma unroll

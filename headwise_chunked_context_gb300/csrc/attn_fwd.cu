@@ -257,9 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) x[c] = -INFINITY;
       }
-      float mx = x[0];
+      // Row max: four independent chains of 3-input max.
+      float mc[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 4; c < 124; c += 8) {
+        mc[0] = fmax3(mc[0], x[c], x[c + 1]);
+        mc[1] = fmax3(mc[1], x[c + 2], x[c + 3]);
+        mc[2] = fmax3(mc[2], x[c + 4], x[c + 5]);
+        mc[3] = fmax3(mc[3], x[c + 6], x[c + 7]);
+      }
+      mc[0] = fmax3(mc[0], x[124], x[125]);
+      mc[1] = fmax3(mc[1], x[126], x[127]);
+      const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
       const float m_new = fmaxf(m_use, mx * sl2);
       const bool need = m_new > m_use + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -282,16 +291,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (need) m_use = m_new;
 
       uint32_t pk0[32], pk1[32];
-      float rs = 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t nmx2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[4] = {0, 0, 0, 0};  // (+0, +0) pairs
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2_approx(fmaf(x[c], sl2, -m_use));
-        const float p1 = ex2_approx(fmaf(x[c + 1], sl2, -m_use));
-        const float p2 = ex2_approx(fmaf(x[64 + c], sl2, -m_use));
-        const float p3 = ex2_approx(fmaf(x[64 + c + 1], sl2, -m_use));
-        rs += (p0 + p1) + (p2 + p3);
+        float t0, t1, t2, t3;
+        f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sl2x2, nmx2), t0, t1);
+        f2_unpack(f2_fma(f2_pack(x[64 + c], x[64 + c + 1]), sl2x2, nmx2), t2, t3);
+        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+        const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
+        acc[(c >> 1) & 1] = f2_add(acc[(c >> 1) & 1], f2_pack(p0, p1));
+        acc[2 + ((c >> 1) & 1)] = f2_add(acc[2 + ((c >> 1) & 1)], f2_pack(p2, p3));
         pk0[c >> 1] = pack_bf16x2(p0, p1);
         pk1[c >> 1] = pack_bf16x2(p2, p3);
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a, b;
+        f2_unpack(acc[i], a, b);
+        rs += a + b;
       }
       l += rs;
       // P over the scores just read (columns [0, 64) of this buffer).

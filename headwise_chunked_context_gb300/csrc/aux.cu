@@ -33,8 +33,8 @@ __global__ void rope_table_kernel(float2* __restrict__ table, int64_t L, const _
 }
 
 // LSE/Delta records for the core backward entry: for head h and row p,
-// Delta = sum_k dO[p, h, k] * O[p, h, k] and LSE * log2(e), stored per
-// 64-row tile as [64 LSE*log2(e) | 64 Delta]; rows past L get +inf / 0.
+// Delta = sum_k dO[p, h, k] * O[p, h, k] and -LSE * log2(e), stored per
+// 64-row tile as [64 -LSE*log2(e) | 64 Delta]; rows past L get -inf / 0.
 // 16 lanes per (row, head): each lane reads 16 bytes of O and of dO.
 __global__ void delta_kernel(const __nv_bfloat16* __restrict__ o, int64_t o_row, int64_t o_head,
                              const __nv_bfloat16* __restrict__ dO, int64_t do_row, int64_t do_head,
@@ -64,7 +64,7 @@ __global__ void delta_kernel(const __nv_bfloat16* __restrict__ o, int64_t o_row,
   for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (live && sub == 0) {
     float* rec = ld + (hh * n_q64 + (row >> 6)) * 128;
-    rec[row & 63] = in ? lse[hh * L + row] * 1.4426950408889634074f : INFINITY;
+    rec[row & 63] = in ? -lse[hh * L + row] * 1.4426950408889634074f : -INFINITY;
     rec[64 + (row & 63)] = in ? acc : 0.f;
   }
 }

@@ -307,11 +307,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           }
         }
-        // LSE/Delta record of this row (padding rows past L get +inf / 0).
+        // LSE/Delta record of this row (padding rows past L get -inf / 0).
         const int n_q64 = (p.L + 63) / 64;
         if (m < n_q64 * 64) {
           float* rec = p.ld_rec + (static_cast<int64_t>(slot) * n_q64 + (m >> 6)) * 128;
-          rec[m & 63] = valid ? p.lse_in[static_cast<int64_t>(slot) * p.L + m] * 1.4426950408889634074f : INFINITY;
+          rec[m & 63] = valid ? -p.lse_in[static_cast<int64_t>(slot) * p.L + m] * 1.4426950408889634074f : -INFINITY;
           rec[64 + (m & 63)] = valid ? dsum : 0.f;
         }
       } else {

@@ -71,7 +71,7 @@ struct Plan {
 };
 
 // LSE/Delta records of the backward: per head of the chunk and 64-query
-// tile, 64 LSE*log2(e) then 64 Delta floats.
+// tile, 64 -LSE*log2(e) then 64 Delta floats.
 size_t ld_records_bytes(const Shape& s) {
   return static_cast<size_t>(s.U) * static_cast<size_t>((s.L + 63) / 64) * 128 * sizeof(float);
 }

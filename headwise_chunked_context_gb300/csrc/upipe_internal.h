@@ -81,8 +81,8 @@ struct AttnBwdParams {
   int nkv;      // KV heads in this launch
   int q_z0, k_z0, v_z0, do_z0;
   // Per local head h and 64-query tile t, a 128-float record at
-  // ld + (h * ceil(L/64) + t) * 128: LSE * log2(e) of the tile's 64 queries
-  // (+inf past L), then their Delta = rowsum(dO * O) (0 past L).
+  // ld + (h * ceil(L/64) + t) * 128: -LSE * log2(e) of the tile's 64 queries
+  // (-inf past L), then their Delta = rowsum(dO * O) (0 past L).
   const float* ld;
   float scale;         // 1/sqrt(d)
   float scale_log2;    // log2(e)/sqrt(d)
