@@ -751,6 +751,7 @@ const char* upipe_strerror(int code) {
     case UPIPE_ERR_CUDA: return "CUDA error";
     case UPIPE_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
     case UPIPE_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
+    case UPIPE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-allocation entry point holds";
   }
   return "unknown error";
 }

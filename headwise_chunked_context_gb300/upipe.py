@@ -24,6 +24,8 @@ UPIPE_ERR_WS_TOO_SMALL = -2
 UPIPE_ERR_CUDA = -3
 UPIPE_ERR_DEVICE_TIMEOUT = -4
 UPIPE_ERR_UNSUPPORTED_DEVICE = -5
+UPIPE_ERR_SCRATCH_LIMIT = -6
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = (
     "upipe_workspace_bytes",
@@ -32,6 +34,7 @@ EXPORTS = (
     "upipe_attn_bwd",
     "upipe_attn_core_fwd",
     "upipe_attn_core_bwd",
+    "upipe_attn_core_bwd_noalloc",
     "upipe_last_device_status",
     "upipe_debug_wait_timeout",
     "upipe_launch_count",
@@ -106,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.upipe_attn_core_fwd.argtypes = [cfgp, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_core_bwd.restype = ctypes.c_int
         L.upipe_attn_core_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_core_bwd_noalloc.restype = ctypes.c_int
+        L.upipe_attn_core_bwd_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P]
         L.upipe_last_device_status.restype = ctypes.c_int
         L.upipe_last_device_status.argtypes = [P]
         L.upipe_debug_wait_timeout.restype = ctypes.c_int
@@ -230,6 +235,20 @@ def attn_core_bwd(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, ws=None, stream=
     _check(lib().upipe_attn_core_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream)),
            "upipe_attn_core_bwd")
+
+
+def attn_core_bwd_noalloc(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, stream=None):
+    """Core backward through the entry point that allocates nothing (its
+    scratch is a fixed array in the library's static device memory; see
+    include/upipe.h).  For callers that may not allocate at call time."""
+    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
+    for t, shp, n in ((do, (L, H, 128), "dout_o"), (dq, (L, H, 128), "dq"), (dk, (L, Hkv, 128), "dk"),
+                      (dv, (L, Hkv, 128), "dv")):
+        _expect(t, shp, torch.bfloat16, n)
+    c = cfg.c()
+    _check(lib().upipe_attn_core_bwd_noalloc(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+           "upipe_attn_core_bwd_noalloc")
 
 
 def last_device_status(stream=None) -> int:

@@ -72,6 +72,7 @@ extern "C" {
 #define UPIPE_ERR_CUDA (-3)               /* a CUDA runtime/driver call failed */
 #define UPIPE_ERR_DEVICE_TIMEOUT (-4)     /* a bounded device wait ran out */
 #define UPIPE_ERR_UNSUPPORTED_DEVICE (-5) /* current device is not sm_103 */
+#define UPIPE_ERR_SCRATCH_LIMIT (-6)      /* needs more than UPIPE_NOALLOC_SCRATCH_BYTES */
 
 /* Problem description.  All fields are read on every call.
  *   L          tokens (1 .. 2^31-1)
@@ -146,6 +147,31 @@ int upipe_attn_core_fwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
 int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq, uint16_t* dk,
                         uint16_t* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Core backward that allocates nothing (no counterpart in the paper; a
+ * convenience of this library).  Same arguments and results as
+ * upipe_attn_core_bwd, minus the workspace.  It is meant for callers that may
+ * not allocate device memory at the point of the call -- for example a
+ * framework's allocator during its own out-of-memory or defragmentation
+ * handling, or a runtime whose device memory budget is reserved up front and
+ * fully claimed.  The scratch (the per-tile LSE/Delta records and, when
+ * U < H/Hkv, the fp32 dK/dV carry) is a fixed array of
+ * UPIPE_NOALLOC_SCRATCH_BYTES in the library's static device memory, which
+ * every GPU that loads the library holds until the process exits.
+ *  - Limit: problems whose upipe_workspace_bytes(cfg, 1, 1, 0) exceeds
+ *    UPIPE_NOALLOC_SCRATCH_BYTES return UPIPE_ERR_SCRATCH_LIMIT before any
+ *    GPU work (for example U = 1, Hkv = 1 fits up to about L = 32K tokens;
+ *    U >= H/Hkv with U = 8 up to about L = 512K).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams, no ordering) race.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.           */
+#define UPIPE_NOALLOC_SCRATCH_BYTES (32u << 20)
+int upipe_attn_core_bwd_noalloc(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq,
+                                uint16_t* dk, uint16_t* dv, void* stream);
 
 /* Synchronizes `stream`, then reads and clears the device status word of
  * the current device.  Returns UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT if a
