@@ -148,6 +148,21 @@ def cpu_oracle_sample(L):
     return 7.0 * L * L * 128 / dt / 1e12, dt
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over all ranks (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_step_per_rank / (ms_per_step / 1e3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -276,17 +291,13 @@ def run_upipe(args, w, world, rank, local):
     code = upipe.last_device_status(stream)
     if code != 0:
         raise RuntimeError(f"device status after timed steps: {upipe.strerror(code)}")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     peak_alloc = torch.cuda.max_memory_allocated(dev) - base_alloc
 
     attn_f, proj_f = layer_flops(L, D, H, Hkv)
     step_flops = attn_f + proj_f
     ms_step = ms / args.steps
-    value = world * step_flops / (ms_step / 1e3) / 1e12
+    value = job_tflops(step_flops, ms_step, world)
     burst, sustained, hbm, peak_src = peaks()
 
     # ---- roofline of the dominant kernel, from the live per-launch events
