@@ -24,6 +24,9 @@
 // the query tile's LSE/Delta record), warp 9 issues tcgen05.mma, and warps 0-7
 // turn scores into P / dS: two warps share each TMEM lane quadrant and split
 // the columns, so every SM sub-partition has two of them to hide latency.
+// The tensor core reads shared-memory operands at about 128 B/clk per SM, so
+// the softmax tiles (P^T, dS^T, dS) stay in TMEM and feed the products that
+// consume them as TMEM A operands.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -95,39 +98,39 @@ __device__ __forceinline__ void pds_slice(const uint32_t (&sv)[32], const uint32
 
 // ============================================================== dQ kernel
 //
-// KV blocks of 64 keys stream through a 4-stage ring; the scores S and dP of
-// block j live in one of two TMEM buffers and dS in one of two shared tiles,
-// so the tensor core computes S/dP of block j+1 while the compute warps turn
-// block j into dS.
+// Q and dO are copied into TMEM once, so S = Q K^T and dP = dO V^T read only
+// K and V from shared memory.  KV blocks of 64 keys stream through a 5-stage
+// ring; S and dP of block j live in TMEM buffer j & 1; the compute warps
+// write dS over the S columns they have read (packed bf16) and dQ += dS K
+// takes dS straight from TMEM, so nothing goes back through shared memory.
 
 namespace dq {
 constexpr int kTileQ = 128 * 128 * 2;   // Q or dO: [128 queries][128 d]
-constexpr int kHalfQ = kTileQ / 2;
 constexpr int kTileK = 64 * 128 * 2;    // K or V block: [64 keys][128 d]
 constexpr int kHalfK = kTileK / 2;
-constexpr int kTileS = 128 * 64 * 2;    // dS: [128 queries][64 keys]
-constexpr int kStages = 4;              // K/V ring depth
+constexpr int kStages = 5;              // K/V ring depth
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTileQ;
 constexpr int OFF_KV = OFF_DO + kTileQ;  // per stage: K then V
-constexpr int OFF_DS = OFF_KV + kStages * 2 * kTileK;  // 2 buffers
-constexpr int OFF_BAR = OFF_DS + 2 * kTileS;
+constexpr int OFF_BAR = OFF_KV + kStages * 2 * kTileK;
 enum {
   B_QDO_FULL,
+  B_QDO_TMEM,  // Q and dO copied into TMEM by the compute warps
   B_KV_FULL,
   B_KV_EMPTY = B_KV_FULL + kStages,
   B_SDP_FULL = B_KV_EMPTY + kStages,
-  B_SDP_EMPTY = B_SDP_FULL + 2,
-  B_DS_FULL = B_SDP_EMPTY + 2,
-  B_DS_EMPTY = B_DS_FULL + 2,
-  B_DQ_DONE = B_DS_EMPTY + 2,
+  B_DS_FULL = B_SDP_FULL + 2,
+  B_SDP_FREE = B_DS_FULL + 2,  // dQ of that buffer done: S/dS and dP columns free
+  B_DQ_DONE = B_SDP_FREE + 2,
   B_DRAIN,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
 constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
-constexpr int TM_S = 0, TM_DP = 128, TM_DQ = 256;  // S, dP: two 64-column buffers each
+// TMEM columns: Q, dO packed bf16 (64 each); S and dP: two 64-column buffers
+// each (dS of a block overwrites its own S buffer); dQ accumulator.
+constexpr int TM_Q = 0, TM_DO = 64, TM_S = 128, TM_DP = 256, TM_DQ = 384;
 }  // namespace dq
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -151,15 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QDO_FULL), 1);
+    mbar_init(bar(B_QDO_TMEM), kComputeWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_SDP_FULL + b), 1);
-      mbar_init(bar(B_SDP_EMPTY + b), kComputeWarps);
       mbar_init(bar(B_DS_FULL + b), kComputeWarps);
-      mbar_init(bar(B_DS_EMPTY + b), 1);
+      mbar_init(bar(B_SDP_FREE + b), 1);
     }
     mbar_init(bar(B_DQ_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
@@ -183,10 +186,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&mdo);
       mbar_expect_tx(bar(B_QDO_FULL), 2 * kTileQ);
       tma_load_3d(sb + OFF_Q, &mq, bar(B_QDO_FULL), 0, qb * 128, p.q_z0 + h);
-      tma_load_3d(sb + OFF_Q + kHalfQ, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
+      tma_load_3d(sb + OFF_Q + kTileQ / 2, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
       tma_load_3d(sb + OFF_DO, &mdo, bar(B_QDO_FULL), 0, qb * 128, p.do_z0 + h);
-      tma_load_3d(sb + OFF_DO + kHalfQ, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
-      int last[kStages] = {-1, -1, -1, -1};
+      tma_load_3d(sb + OFF_DO + kTileQ / 2, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
+      int last[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last[s] = -1;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
@@ -207,14 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S = Q K^T, dP = dO V^T
-      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dQ += dS K (K as MN-major B)
+      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S = Q K^T, dP = dO V^T (A from TMEM)
+      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dQ += dS K (dS from TMEM, K MN-major)
       // Event-driven issue: S/dP of block ns once its K/V stage has landed
-      // and the compute warps have read block ns - 2 out of the TMEM buffer;
-      // dQ += dS K of block nq once its dS tile is written.
+      // and dQ of block ns - 2 (which used the same TMEM buffers) is done;
+      // dQ += dS K of block nq once the compute warps have written its dS.
       auto sdp_ready = [&](int j) {
         return mbar_test(bar(B_KV_FULL + j % kStages), (j / kStages) & 1) &&
-               mbar_test(bar(B_SDP_EMPTY + (j & 1)), ((j >> 1) & 1) ^ 1);
+               mbar_test(bar(B_SDP_FREE + (j & 1)), ((j >> 1) & 1) ^ 1);
       };
       auto dq_ready = [&](int j) { return mbar_test(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
       auto issue_sdp = [&](int j) {
@@ -223,17 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t va = ka + kTileK;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t qo = (kk >> 2) * kHalfQ + (kk & 3) * 32;
           const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
-          umma_bf16(tmem + TM_S + b * 64, sdesc_sw128(sb + OFF_Q + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024),
-                    id_s, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + TM_S + b * 64, tmem + TM_Q + kk * 8, sdesc_sw128(ka + ko, 16, 1024), id_s,
+                       kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t qo = (kk >> 2) * kHalfQ + (kk & 3) * 32;
           const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
-          umma_bf16(tmem + TM_DP + b * 64, sdesc_sw128(sb + OFF_DO + qo, 16, 1024), sdesc_sw128(va + ko, 16, 1024),
-                    id_s, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + TM_DP + b * 64, tmem + TM_DO + kk * 8, sdesc_sw128(va + ko, 16, 1024), id_s,
+                       kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(B_SDP_FULL + b));
       };
@@ -241,16 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         const int st = j % kStages;
         const uint32_t ka = sb + OFF_KV + st * 2 * kTileK;
-        const uint32_t da = sb + OFF_DS + b * kTileS;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + TM_DQ, sdesc_sw128(da + kk * 32, 16, 1024), sdesc_sw128(ka + kk * 2048, kHalfK, 1024),
-                    id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          // keys 16 kk .. 16 kk + 15: written by compute half kk / 2 at its
+          // own 32-column slice of the S buffer
+          const uint32_t a = tmem + TM_S + b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+          umma_bf16_ts(tmem + TM_DQ, a, sdesc_sw128(ka + kk * 2048, kHalfK, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_DS_EMPTY + b));
+        umma_commit(bar(B_SDP_FREE + b));
         umma_commit(bar(B_KV_EMPTY + st));
       };
-      bool ok = mbar_wait(bar(B_QDO_FULL), 0, w);
+      bool ok = mbar_wait(bar(B_QDO_TMEM), 0, w);
+      tc_fence_after();
       int ns = 0, nq = 0;
       Watchdog wd;
       wd.reset();
@@ -287,8 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* rec = p.ld + (static_cast<int64_t>(h) * n_q64 + (qpos >> 6)) * 128;
     const float nlse2 = valid ? rec[qpos & 63] : 0.f;  // -LSE * log2(e)
     const float dlt = valid ? rec[64 + (qpos & 63)] : 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    bool ok = warp_wait(bar(B_QDO_FULL), 0, w);
+    if (ok) {  // half 0 copies the Q row into TMEM, half 1 the dO row
+      tile_row_to_tmem(sb + (half == 0 ? OFF_Q : OFF_DO), r, trow + (half == 0 ? TM_Q : TM_DO));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QDO_TMEM));
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
       const int b = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!(ok = warp_wait(bar(B_SDP_FULL + b), ph, w))) break;
@@ -298,22 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(trow + TM_DP + b * 64 + half * 32, dv);
       tmem_ld_wait(sv);
       tmem_ld_wait(dv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY + b));
       const int k0 = j * 64 + half * 32;  // key of this warp's first column
       uint32_t pk[16];
       if (j >= 2 * qb)  // the diagonal tile (warp-uniform)
         ds_slice<true>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
       else
         ds_slice<false>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
-      if (!(ok = warp_wait(bar(B_DS_EMPTY + b), ph ^ 1, w))) break;
-      const uint32_t da = sb + OFF_DS + b * kTileS;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        st_shared_v4(da + sw128_offset(r, half * 4 + ch), pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                     pk[4 * ch + 3]);
-      fence_async_smem();
+      // dS over the first 16 of the 32 S columns this warp just read.
+      tmem_st16(trow + TM_S + b * 64 + half * 32, pk);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS_FULL + b));
     }
@@ -361,31 +367,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================ dK/dV kernel
+//
+// S^T and dP^T of a 64-query tile live in TMEM buffer it & 1; the compute
+// warps write P^T and dS^T (packed bf16) over the columns they have read,
+// and dV += P^T dO, dK += dS^T Q take them straight from TMEM.  Q/dO tiles
+// and their LSE/Delta records stream through a 4-stage ring.
 
 namespace dkv {
 constexpr int kKV = 128 * 128 * 2;  // K or V tile: [128 keys][128 d]
 constexpr int kKVHalf = kKV / 2;
 constexpr int kQ = 64 * 128 * 2;    // Q or dO tile: [64 queries][128 d]
 constexpr int kQHalf = kQ / 2;
-constexpr int kPT = 128 * 64 * 2;   // P^T or dS^T tile: [128 keys][64 queries]
+constexpr int kStages = 4;          // Q/dO ring depth
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKV;
-constexpr int kStages = 3;                 // Q/dO ring depth
-constexpr int OFF_Q = OFF_V + kKV;         // kStages stages
+constexpr int OFF_Q = OFF_V + kKV;             // kStages stages
 constexpr int OFF_DO = OFF_Q + kStages * kQ;
-constexpr int OFF_PT = OFF_DO + kStages * kQ;  // 2 buffers
-constexpr int OFF_DST = OFF_PT + 2 * kPT;      // 2 buffers
-constexpr int OFF_LD = OFF_DST + 2 * kPT;      // per stage: the tile's LSE/Delta record
+constexpr int OFF_LD = OFF_DO + kStages * kQ;  // per stage: the tile's LSE/Delta record
 constexpr int OFF_BAR = OFF_LD + kStages * 512;
 enum {
   B_KV_FULL,
   B_QDO_FULL,
   B_QDO_EMPTY = B_QDO_FULL + kStages,
   B_SDP_FULL = B_QDO_EMPTY + kStages,
-  B_SDP_EMPTY = B_SDP_FULL + 2,
-  B_PDS_FULL = B_SDP_EMPTY + 2,
-  B_PDS_EMPTY = B_PDS_FULL + 2,
-  B_CARRY_READY = B_PDS_EMPTY + 2,
+  B_PDS_FULL = B_SDP_FULL + 2,
+  B_SDP_FREE = B_PDS_FULL + 2,  // dV/dK of that buffer done: S^T/P^T and dP^T/dS^T columns free
+  B_CARRY_READY = B_SDP_FREE + 2,
   B_DKV_DONE,
   B_DRAIN,
   B_COUNT
@@ -423,11 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_QDO_FULL + s), 1);
       mbar_init(bar(B_QDO_EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_SDP_FULL + s), 1);
-      mbar_init(bar(B_SDP_EMPTY + s), kComputeWarps);
-      mbar_init(bar(B_PDS_FULL + s), kComputeWarps);
-      mbar_init(bar(B_PDS_EMPTY + s), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_SDP_FULL + b), 1);
+      mbar_init(bar(B_PDS_FULL + b), kComputeWarps);
+      mbar_init(bar(B_SDP_FREE + b), 1);
     }
     mbar_init(bar(B_CARRY_READY), kComputeWarps);
     mbar_init(bar(B_DKV_DONE), 1);
@@ -448,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q and dO tiles (TMA) plus the tile's LSE/Delta record (bulk copy), all
     // on one barrier per stage.
     if (lane == 0) {
-      int last[kStages] = {-1, -1, -1};
+      int last[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last[s] = -1;
       tma_prefetch_map(&mq);
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
@@ -482,17 +490,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
-      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // dV += P^T dO, dK += dS^T Q
+      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // dV += P^T dO, dK += dS^T Q (A from TMEM)
       // Event-driven issue: S^T/dP^T of tile ns once its Q/dO stage has
-      // landed and the compute warps have read tile ns - 2 out of the TMEM
-      // buffer; dV/dK products of tile ng once its P^T/dS^T tiles are written.
+      // landed and the dV/dK products of tile ns - 2 (which read the same
+      // TMEM buffers) are done; dV/dK of tile ng once P^T/dS^T are written.
       auto sdp_ready = [&](int it) {
         return mbar_test(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1) &&
-               mbar_test(bar(B_SDP_EMPTY + (it & 1)), ((it >> 1) & 1) ^ 1);
+               mbar_test(bar(B_SDP_FREE + (it & 1)), ((it >> 1) & 1) ^ 1);
       };
       auto grad_ready = [&](int it) { return mbar_test(bar(B_PDS_FULL + (it & 1)), (it >> 1) & 1); };
       auto issue_sdp = [&](int it) {
-        const int s = it & 1;
+        const int b = it & 1;
         const int qs = it % kStages;
         const uint32_t qa = sb + OFF_Q + qs * kQ;
         const uint32_t da = sb + OFF_DO + qs * kQ;
@@ -500,36 +508,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
           const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_ST + s * 64, sdesc_sw128(sb + OFF_K + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024),
+          umma_bf16(tmem + TM_ST + b * 64, sdesc_sw128(sb + OFF_K + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024),
                     id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
           const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_DPT + s * 64, sdesc_sw128(sb + OFF_V + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024),
+          umma_bf16(tmem + TM_DPT + b * 64, sdesc_sw128(sb + OFF_V + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024),
                     id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_SDP_FULL + s));
+        umma_commit(bar(B_SDP_FULL + b));
       };
       auto issue_grad = [&](int it) {
-        const int s = it & 1;
+        const int b = it & 1;
         const int qs = it % kStages;
-        const uint32_t pt = sb + OFF_PT + s * kPT;
-        const uint32_t dst = sb + OFF_DST + s * kPT;
         const uint32_t qa = sb + OFF_Q + qs * kQ;
         const uint32_t da = sb + OFF_DO + qs * kQ;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + TM_DV, sdesc_sw128(pt + kk * 32, 16, 1024), sdesc_sw128(da + kk * 2048, kQHalf, 1024),
-                    id_g, (carry_in || it > 0 || kk > 0) ? 1u : 0u);
+          // queries 16 kk .. 16 kk + 15: written by compute half kk / 2
+          const uint32_t col = b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+          umma_bf16_ts(tmem + TM_DV, tmem + TM_ST + col, sdesc_sw128(da + kk * 2048, kQHalf, 1024), id_g,
+                       (carry_in || it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + TM_DK, sdesc_sw128(dst + kk * 32, 16, 1024), sdesc_sw128(qa + kk * 2048, kQHalf, 1024),
-                    id_g, (carry_in || it > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t col = b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+          umma_bf16_ts(tmem + TM_DK, tmem + TM_DPT + col, sdesc_sw128(qa + kk * 2048, kQHalf, 1024), id_g,
+                       (carry_in || it > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_PDS_EMPTY + s));
+        umma_commit(bar(B_SDP_FREE + b));
         umma_commit(bar(B_QDO_EMPTY + qs));
       };
       bool ok = mbar_wait(bar(B_KV_FULL), 0, w);
@@ -567,8 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
     const float sl2 = p.scale_log2;
     // Warps 0-3 own dK, warps 4-7 own dV (carry load and epilogue).
-    float* my_carry =
-        p.dkv_carry + (static_cast<int64_t>(kv * 2 + half) * p.L + kpos) * kHeadDim;
+    float* my_carry = p.dkv_carry + (static_cast<int64_t>(kv * 2 + half) * p.L + kpos) * kHeadDim;
     const int my_col = half == 0 ? TM_DK : TM_DV;
     bool ok = true;
     if (carry_in) {
@@ -591,20 +599,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_CARRY_READY));
     }
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
+      const int b = it & 1;
       const uint32_t ph = (it >> 1) & 1;
+      const int qs = it % kStages;
       const int qi = 2 * kb + it % nqi;
-      if (!(ok = warp_wait(bar(B_SDP_FULL + s), ph, w))) break;
+      if (!(ok = warp_wait(bar(B_SDP_FULL + b), ph, w))) break;
       tc_fence_after();
       uint32_t sv[32], dv[32];
-      tmem_ld32(trow + TM_ST + s * 64 + half * 32, sv);
-      tmem_ld32(trow + TM_DPT + s * 64 + half * 32, dv);
+      tmem_ld32(trow + TM_ST + b * 64 + half * 32, sv);
+      tmem_ld32(trow + TM_DPT + b * 64 + half * 32, dv);
       tmem_ld_wait(sv);
       tmem_ld_wait(dv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SDP_EMPTY + s));
-      const int qs = it % kStages;
       if (!(ok = warp_wait(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
       const float4* l4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + half * 32);
       const float4* d4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + 64 + half * 32);
@@ -614,19 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         pds_slice<true>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
       else
         pds_slice<false>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
-      if (!(ok = warp_wait(bar(B_PDS_EMPTY + s), ph ^ 1, w))) break;
-      const uint32_t pt = sb + OFF_PT + s * kPT;
-      const uint32_t dst = sb + OFF_DST + s * kPT;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        st_shared_v4(pt + sw128_offset(r, half * 4 + ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
-                     pp[4 * ch + 3]);
-        st_shared_v4(dst + sw128_offset(r, half * 4 + ch), dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
-                     dd[4 * ch + 3]);
-      }
-      fence_async_smem();
+      // P^T and dS^T over the first 16 of the 32 columns this warp just read.
+      tmem_st16(trow + TM_ST + b * 64 + half * 32, pp);
+      tmem_st16(trow + TM_DPT + b * 64 + half * 32, dd);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PDS_FULL + s));
+      if (lane == 0) mbar_arrive(bar(B_PDS_FULL + b));
     }
     if (ok) ok = warp_wait(bar(B_DKV_DONE), 0, w);
     if (ok) {

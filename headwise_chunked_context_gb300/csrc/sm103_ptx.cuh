@@ -295,7 +295,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       UPIPE_S8(0), UPIPE_S8(8), UPIPE_S8(16), UPIPE_S8(24)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Copies this thread's 128-element bf16 row of a [128][128] tile that TMA
+// wrote with 128-byte swizzle (two 64-column halves of 16 KB) into 64 TMEM
+// columns as packed pairs -- the layout tcgen05.mma reads an A operand in.
+__device__ __forceinline__ void tile_row_to_tmem(uint32_t tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int hq = 0; hq < 2; ++hq) {
+    uint32_t q[32];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t a = tile + hq * 16384 + static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(q[4 * ch]), "=r"(q[4 * ch + 1]), "=r"(q[4 * ch + 2]), "=r"(q[4 * ch + 3])
+                   : "r"(a));
+    }
+    tmem_st32(taddr + hq * 32, q);
+  }
+}
 
 // ------------------------------------------------------------------ misc
 

@@ -39,6 +39,14 @@ Readings of points the pages leave open (each also listed in the design doc):
 Every function below is plain: library matmuls and elementwise NumPy, no
 blocking beyond streaming query rows against the full K/V (which changes no
 arithmetic that matters at fp64), no fusion.
+
+Precision model ("bf16 in / fp32 accumulate").  By default everything is
+exact fp64.  With ``bf16_tensors=True`` the layer functions round, at the
+points where a bf16 implementation stores them, the tensors that are bf16
+inputs of the next contraction -- Q and K after RoPE, V, the attention output
+O, and dO = dout Wo -- to the nearest bfloat16 (``bf16_round``); every
+product and sum stays exact fp64.  This isolates an implementation's own
+arithmetic from the rounding that the bf16 storage itself implies.
 """
 
 from __future__ import annotations
@@ -46,6 +54,18 @@ from __future__ import annotations
 import numpy as np
 
 F64 = np.float64
+
+
+def bf16_round(a) -> np.ndarray:
+    """Nearest bfloat16 (ties to even) of ``a``, returned as fp64.
+
+    The value is first rounded to fp32 (as an fp32 accumulator holds it),
+    then its fp32 bit pattern is rounded to the upper 16 bits.
+    """
+    a32 = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = a32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(F64)
 
 
 # ---------------------------------------------------------------------------
@@ -247,20 +267,29 @@ def attention_dkv_tail(q_tail, k_tail, v_tail, do_tail, o_tail, lse_tail, scale)
 # The layer: plain (all heads at once) definition.
 # ---------------------------------------------------------------------------
 
-def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None):
+def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None, bf16_tensors=False):
     """out [L, D], LSE [H, L], O [L, H, d] of one GQA/RoPE attention layer."""
     x = np.asarray(x, dtype=F64)
     Wo = np.asarray(Wo, dtype=F64)
     if d is None:
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
+    if bf16_tensors:
+        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
     o, lse = attention_core_fwd(q, k, v)
+    if bf16_tensors:
+        o = bf16_round(o)
     out = o.reshape(x.shape[0], H * d) @ Wo.T
     return out, lse, o
 
 
-def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None):
-    """dx [L, D], dWqkv [(H+2Hkv)d, D], dWo [D, H d]: gradient of sum(out*dout)."""
+def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_tensors=False):
+    """dx [L, D], dWqkv [(H+2Hkv)d, D], dWo [D, H d]: gradient of sum(out*dout).
+
+    With ``bf16_tensors`` the gradient is the one of the bf16-materialised
+    layer (see the module header): Q, K, V, O and dO are rounded to bf16
+    where they are stored; the rounding itself is treated as the identity.
+    """
     x = np.asarray(x, dtype=F64)
     Wqkv = np.asarray(Wqkv, dtype=F64)
     Wo = np.asarray(Wo, dtype=F64)
@@ -269,10 +298,16 @@ def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None):
     if d is None:
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
+    if bf16_tensors:
+        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
     o, lse = attention_core_fwd(q, k, v)
+    if bf16_tensors:
+        o = bf16_round(o)
     o_flat = o.reshape(L, H * d)
     dWo = dout.T @ o_flat
     do = (dout @ Wo).reshape(L, H, d)
+    if bf16_tensors:
+        do = bf16_round(do)
     dq, dk, dv = attention_core_bwd(q, k, v, o, lse, do)
     pos = np.arange(L)
     dq = rope_apply(dq, pos, theta, inverse=True)

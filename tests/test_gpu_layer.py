@@ -1,7 +1,10 @@
 """GPU parity of the whole head-chunked layer (projections, RoPE, causal
 attention, output projection; forward and backward) against the fp64
 oracle, through the C ABI, and bit-exactness of every chunk size against
-the unchunked run (U = H)."""
+the unchunked run (U = H).  The oracle runs in its bf16-materialisation mode:
+Q, K, V, O and dO -- the tensors a bf16 layer stores and feeds to its next
+contraction -- are rounded to bf16 where they are stored; all products and
+sums stay exact fp64."""
 
 import numpy as np
 import pytest
@@ -34,10 +37,10 @@ def _run(shape, U, keep_o=False):
 def _check_vs_oracle(shape, inputs, outs):
     x, wqkv, wo, dout = (f64(t) for t in inputs)
     out, lse, dx, dwqkv, dwo = outs
-    rout, rlse, _ = orc.layer_fwd(x, wqkv, wo, shape.H, shape.Hkv, shape.theta)
+    rout, rlse, _ = orc.layer_fwd(x, wqkv, wo, shape.H, shape.Hkv, shape.theta, bf16_tensors=True)
     assert_close(f64(out), rout, "out")
     assert_close(f64(lse), rlse, "lse")
-    rdx, rdwqkv, rdwo = orc.layer_bwd(x, wqkv, wo, dout, shape.H, shape.Hkv, shape.theta)
+    rdx, rdwqkv, rdwo = orc.layer_bwd(x, wqkv, wo, dout, shape.H, shape.Hkv, shape.theta, bf16_tensors=True)
     assert_close(f64(dx), rdx, "dx")
     assert_close(f64(dwqkv), rdwqkv, "dWqkv", weight_grad=True)
     assert_close(f64(dwo), rdwo, "dWo", weight_grad=True)

@@ -329,3 +329,37 @@ def test_intermediate_memory_ratio():
     assert 1 - r == pytest.approx(0.875, abs=0)
     # U < g: each chunk still needs its one KV head.
     assert orc.intermediate_bytes(1024, 2, 8, 2, 128) == 1024 * 128 * 2 * (4 + 2)
+
+
+# ----------------------------------------------------- bf16 precision model
+
+def test_bf16_round_matches_library_conversion():
+    rng = np.random.default_rng(12)
+    a = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, -1.0, 3.0e38, 1e-40]])
+    # exact ties: 1 + 2^-8 (tie, even stays at 1) and 1 + 3*2^-8 (tie, rounds up)
+    a = np.concatenate([a, [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8)]])
+    want = torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(orc.bf16_round(a), want)
+    assert orc.bf16_round(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    assert orc.bf16_round(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+
+
+def test_bf16_materialised_layer_is_the_exact_layer_on_rounded_tensors():
+    """With bf16_tensors the forward equals the exact forward fed with the
+    rounded Q/K/V and rounded O, and differs from the exact layer only at the
+    bf16 level."""
+    x, Wqkv, Wo, dout, H, Hkv, theta = _micro(seed=3, L=24, D=32)
+    out_b, lse_b, o_b = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta, bf16_tensors=True)
+    d = Wo.shape[1] // H
+    q, k, v = orc.project_qkv(x, Wqkv, H, Hkv, d, theta)
+    o, lse = orc.attention_core_fwd(orc.bf16_round(q), orc.bf16_round(k), orc.bf16_round(v))
+    np.testing.assert_allclose(lse_b, lse, atol=1e-13)
+    np.testing.assert_allclose(out_b, orc.bf16_round(o).reshape(x.shape[0], -1) @ Wo.T, atol=1e-13)
+    out, _, _ = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta)
+    rel = np.linalg.norm(out_b - out) / np.linalg.norm(out)
+    assert 1e-5 < rel < 1e-2
+    dx_b, dW_b, dWo_b = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, bf16_tensors=True)
+    dx, dW, dWo = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta)
+    for a, b in ((dx_b, dx), (dW_b, dW), (dWo_b, dWo)):
+        assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-2

@@ -51,3 +51,12 @@ def assert_close(got, ref, name, weight_grad=False):
     assert scaled <= MAX_ABS, f"{name}: scaled max-abs {scaled:.3e} (raw {max_abs:.3e}) > {MAX_ABS}"
     assert rel <= REL_L2, f"{name}: rel-L2 {rel:.3e} > {REL_L2}"
     return max_abs, rel
+
+
+def assert_max_abs(got, ref, name, weight_grad=False):
+    """Element-wise bound only (for hand-picked edge rows, which are not a
+    uniform sample of the tensor and so say nothing about its rel-L2)."""
+    scaled = scaled_max_abs(got, ref, weight_grad)
+    assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{name}: non-finite values"
+    assert scaled <= MAX_ABS, f"{name}: scaled max-abs {scaled:.3e} > {MAX_ABS}"
+    return scaled
