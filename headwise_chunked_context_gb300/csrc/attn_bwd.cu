@@ -11,7 +11,7 @@
 //
 // Two kernels, neither using atomics, so every result has one fixed fp32
 // summation order that does not depend on the chunk size U:
-//  * dq kernel: one CTA per (query head, 128-query tile) walks its 64-key
+//  * dq kernel: one CTA per (query head, 128-query tile) walks its 128-key
 //    blocks in ascending order and accumulates dQ in TMEM;
 //  * dkdv kernel: one CTA per (KV head, 128-key tile) walks the query heads
 //    that read this KV head (ascending) and, for each, the 64-query tiles at
@@ -98,39 +98,41 @@ __device__ __forceinline__ void pds_slice(const uint32_t (&sv)[32], const uint32
 
 // ============================================================== dQ kernel
 //
-// Q and dO are copied into TMEM once, so S = Q K^T and dP = dO V^T read only
-// K and V from shared memory.  KV blocks of 64 keys stream through a 5-stage
-// ring; S and dP of block j live in TMEM buffer j & 1; the compute warps
-// write dS over the S columns they have read (packed bf16) and dQ += dS K
-// takes dS straight from TMEM, so nothing goes back through shared memory.
+// KV blocks of 128 keys, so every product is an M=128, N=128 tcgen05.mma.
+// S = Q K^T goes into one of two TMEM buffers; dP = dO V^T into one buffer
+// that the compute warps release as soon as they have read it; the compute
+// warps write dS (packed bf16) over the S columns they have read, and
+// dQ += dS K takes dS straight from TMEM.  K and V stream through separate
+// two-stage TMA rings (V is released after dP, K after dQ).
 
 namespace dq {
-constexpr int kTileQ = 128 * 128 * 2;   // Q or dO: [128 queries][128 d]
-constexpr int kTileK = 64 * 128 * 2;    // K or V block: [64 keys][128 d]
-constexpr int kHalfK = kTileK / 2;
-constexpr int kStages = 5;              // K/V ring depth
+constexpr int kTile = 128 * 128 * 2;   // [128][128] bf16 as two 64-column halves
+constexpr int kHalf = kTile / 2;
+constexpr int kStages = 2;
 constexpr int OFF_Q = 0;
-constexpr int OFF_DO = OFF_Q + kTileQ;
-constexpr int OFF_KV = OFF_DO + kTileQ;  // per stage: K then V
-constexpr int OFF_BAR = OFF_KV + kStages * 2 * kTileK;
+constexpr int OFF_DO = OFF_Q + kTile;
+constexpr int OFF_K = OFF_DO + kTile;             // kStages
+constexpr int OFF_V = OFF_K + kStages * kTile;    // kStages
+constexpr int OFF_BAR = OFF_V + kStages * kTile;
 enum {
   B_QDO_FULL,
-  B_QDO_TMEM,  // Q and dO copied into TMEM by the compute warps
-  B_KV_FULL,
-  B_KV_EMPTY = B_KV_FULL + kStages,
-  B_SDP_FULL = B_KV_EMPTY + kStages,
-  B_DS_FULL = B_SDP_FULL + 2,
-  B_SDP_FREE = B_DS_FULL + 2,  // dQ of that buffer done: S/dS and dP columns free
-  B_DQ_DONE = B_SDP_FREE + 2,
+  B_K_FULL,
+  B_K_EMPTY = B_K_FULL + kStages,
+  B_V_FULL = B_K_EMPTY + kStages,
+  B_V_EMPTY = B_V_FULL + kStages,
+  B_S_FULL = B_V_EMPTY + kStages,
+  B_S_FREE = B_S_FULL + 2,   // dQ of that buffer done: its S/dS columns free
+  B_DS_FULL = B_S_FREE + 2,
+  B_DP_FULL = B_DS_FULL + 2,
+  B_DP_EMPTY,                // the compute warps have read dP
+  B_DQ_DONE,
   B_DRAIN,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
 constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
-// TMEM columns: Q, dO packed bf16 (64 each); S and dP: two 64-column buffers
-// each (dS of a block overwrites its own S buffer); dQ accumulator.
-constexpr int TM_Q = 0, TM_DO = 64, TM_S = 128, TM_DP = 256, TM_DQ = 384;
+constexpr int TM_S = 0, TM_DP = 256, TM_DQ = 384;  // S: two 128-column buffers
 }  // namespace dq
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -147,23 +149,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y;
   const int kz = p.k_z0 + h / p.g_loc;
   const int vz = p.v_z0 + h / p.g_loc;
-  const int n_kv = 2 * qb + 2;  // causal: 64-key blocks 0 .. 2 qb + 1
+  const int n_kv = qb + 1;  // causal: 128-key blocks 0 .. qb
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QDO_FULL), 1);
-    mbar_init(bar(B_QDO_TMEM), kComputeWarps);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_KV_FULL + s), 1);
-      mbar_init(bar(B_KV_EMPTY + s), 1);
+      mbar_init(bar(B_K_FULL + s), 1);
+      mbar_init(bar(B_K_EMPTY + s), 1);
+      mbar_init(bar(B_V_FULL + s), 1);
+      mbar_init(bar(B_V_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_SDP_FULL + b), 1);
+      mbar_init(bar(B_S_FULL + b), 1);
+      mbar_init(bar(B_S_FREE + b), 1);
       mbar_init(bar(B_DS_FULL + b), kComputeWarps);
-      mbar_init(bar(B_SDP_FREE + b), 1);
     }
+    mbar_init(bar(B_DP_FULL), 1);
+    mbar_init(bar(B_DP_EMPTY), kComputeWarps);
     mbar_init(bar(B_DQ_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
@@ -184,89 +189,118 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
       tma_prefetch_map(&mdo);
-      mbar_expect_tx(bar(B_QDO_FULL), 2 * kTileQ);
+      mbar_expect_tx(bar(B_QDO_FULL), 2 * kTile);
       tma_load_3d(sb + OFF_Q, &mq, bar(B_QDO_FULL), 0, qb * 128, p.q_z0 + h);
-      tma_load_3d(sb + OFF_Q + kTileQ / 2, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
+      tma_load_3d(sb + OFF_Q + kHalf, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
       tma_load_3d(sb + OFF_DO, &mdo, bar(B_QDO_FULL), 0, qb * 128, p.do_z0 + h);
-      tma_load_3d(sb + OFF_DO + kTileQ / 2, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
-      int last[kStages];
+      tma_load_3d(sb + OFF_DO + kHalf, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
+      int last_k[kStages], last_v[kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last[s] = -1;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        if (!mbar_wait(bar(B_KV_EMPTY + s), ph ^ 1, w)) break;
-        const uint32_t ka = sb + OFF_KV + s * 2 * kTileK;
-        mbar_expect_tx(bar(B_KV_FULL + s), 2 * kTileK);
-        tma_load_3d(ka, &mk, bar(B_KV_FULL + s), 0, j * 64, kz);
-        tma_load_3d(ka + kHalfK, &mk, bar(B_KV_FULL + s), 64, j * 64, kz);
-        tma_load_3d(ka + kTileK, &mv, bar(B_KV_FULL + s), 0, j * 64, vz);
-        tma_load_3d(ka + kTileK + kHalfK, &mv, bar(B_KV_FULL + s), 64, j * 64, vz);
-        last[s] = j;
+      for (int s = 0; s < kStages; ++s) last_k[s] = last_v[s] = -1;
+      // V(j) frees earlier than K(j), so V runs one block ahead of K.
+      int nk = 0, nv = 0;
+      Watchdog wd;
+      wd.reset();
+      bool ok = true;
+      while (ok && (nk < n_kv || nv < n_kv)) {
+        bool did = false;
+        if (nv < n_kv && nv <= nk + 1 &&
+            mbar_test(bar(B_V_EMPTY + nv % kStages), ((nv / kStages) & 1) ^ 1)) {
+          const int s = nv % kStages;
+          mbar_expect_tx(bar(B_V_FULL + s), kTile);
+          tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, nv * 128, vz);
+          tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, nv * 128, vz);
+          last_v[s] = nv++;
+          did = true;
+        }
+        if (nk < n_kv && mbar_test(bar(B_K_EMPTY + nk % kStages), ((nk / kStages) & 1) ^ 1)) {
+          const int s = nk % kStages;
+          mbar_expect_tx(bar(B_K_FULL + s), kTile);
+          tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, nk * 128, kz);
+          tma_load_3d(sb + OFF_K + s * kTile + kHalf, &mk, bar(B_K_FULL + s), 64, nk * 128, kz);
+          last_k[s] = nk++;
+          did = true;
+        }
+        if (did) wd.reset();
+        else ok = wd.alive(w);
       }
       if (*abort_flag) {
         mbar_wait_drain(bar(B_QDO_FULL), 0, p.status);
-        for (int s = 0; s < kStages; ++s)
-          if (last[s] >= 0) mbar_wait_drain(bar(B_KV_FULL + s), (last[s] / kStages) & 1, p.status);
+        for (int s = 0; s < kStages; ++s) {
+          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] / kStages) & 1, p.status);
+          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] / kStages) & 1, p.status);
+        }
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S = Q K^T, dP = dO V^T (A from TMEM)
-      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dQ += dS K (dS from TMEM, K MN-major)
-      // Event-driven issue: S/dP of block ns once its K/V stage has landed
-      // and dQ of block ns - 2 (which used the same TMEM buffers) is done;
-      // dQ += dS K of block nq once the compute warps have written its dS.
-      auto sdp_ready = [&](int j) {
-        return mbar_test(bar(B_KV_FULL + j % kStages), (j / kStages) & 1) &&
-               mbar_test(bar(B_SDP_FREE + (j & 1)), ((j >> 1) & 1) ^ 1);
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);   // dQ += dS K (dS from TMEM, K MN-major)
+      // Event-driven issue of three product kinds: S(ns) once K(ns) has
+      // landed and dQ(ns - 2) has released the buffer; dP(nd) once V(nd) has
+      // landed and dP(nd - 1) has been read; dQ(nq) once dS(nq) is written.
+      auto s_ready = [&](int j) {
+        return mbar_test(bar(B_K_FULL + j % kStages), (j / kStages) & 1) &&
+               mbar_test(bar(B_S_FREE + (j & 1)), ((j >> 1) & 1) ^ 1);
+      };
+      auto dp_ready = [&](int j) {
+        return mbar_test(bar(B_V_FULL + j % kStages), (j / kStages) & 1) &&
+               mbar_test(bar(B_DP_EMPTY), (j & 1) ^ 1);
       };
       auto dq_ready = [&](int j) { return mbar_test(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
-      auto issue_sdp = [&](int j) {
-        const int b = j & 1;
-        const uint32_t ka = sb + OFF_KV + (j % kStages) * 2 * kTileK;
-        const uint32_t va = ka + kTileK;
+      auto issue_s = [&](int j) {
+        const uint32_t ka = sb + OFF_K + (j % kStages) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
-          umma_bf16_ts(tmem + TM_S + b * 64, tmem + TM_Q + kk * 8, sdesc_sw128(ka + ko, 16, 1024), id_s,
-                       kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + TM_S + (j & 1) * 128, sdesc_sw128(sb + OFF_Q + off, 16, 1024),
+                    sdesc_sw128(ka + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
         }
+        umma_commit(bar(B_S_FULL + (j & 1)));
+      };
+      auto issue_dp = [&](int j) {
+        const int s = j % kStages;
+        const uint32_t va = sb + OFF_V + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * kHalfK + (kk & 3) * 32;
-          umma_bf16_ts(tmem + TM_DP + b * 64, tmem + TM_DO + kk * 8, sdesc_sw128(va + ko, 16, 1024), id_s,
-                       kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + TM_DP, sdesc_sw128(sb + OFF_DO + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), id_kk,
+                    kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_SDP_FULL + b));
+        umma_commit(bar(B_DP_FULL));
+        umma_commit(bar(B_V_EMPTY + s));
       };
       auto issue_dq = [&](int j) {
         const int b = j & 1;
-        const int st = j % kStages;
-        const uint32_t ka = sb + OFF_KV + st * 2 * kTileK;
+        const int s = j % kStages;
+        const uint32_t ka = sb + OFF_K + s * kTile;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // keys 16 kk .. 16 kk + 15: written by compute half kk / 2 at its
-          // own 32-column slice of the S buffer
-          const uint32_t a = tmem + TM_S + b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + TM_DQ, a, sdesc_sw128(ka + kk * 2048, kHalfK, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          // keys 16 kk .. 16 kk + 15: compute half kk / 4 wrote them at its own
+          // 64-column slice of the S buffer
+          const uint32_t a = tmem + TM_S + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_bf16_ts(tmem + TM_DQ, a, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_SDP_FREE + b));
-        umma_commit(bar(B_KV_EMPTY + st));
+        umma_commit(bar(B_S_FREE + b));
+        umma_commit(bar(B_K_EMPTY + s));
       };
-      bool ok = mbar_wait(bar(B_QDO_TMEM), 0, w);
-      tc_fence_after();
-      int ns = 0, nq = 0;
+      bool ok = mbar_wait(bar(B_QDO_FULL), 0, w);
+      int ns = 0, nd = 0, nq = 0;
       Watchdog wd;
       wd.reset();
       while (ok && nq < n_kv) {
         bool did = false;
-        if (ns < n_kv && sdp_ready(ns)) {
+        if (ns < n_kv && ns <= nd + 1 && s_ready(ns)) {
           tc_fence_after();
-          issue_sdp(ns++);
+          issue_s(ns++);
           did = true;
         }
-        if (nq < ns && dq_ready(nq)) {
+        if (nd < ns && dp_ready(nd)) {
+          tc_fence_after();
+          issue_dp(nd++);
+          did = true;
+        }
+        if (nq < nd && dq_ready(nq)) {
           tc_fence_after();
           issue_dq(nq++);
           did = true;
@@ -280,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // Compute warps: quadrant (warp & 3) of the TMEM lanes = query rows,
-    // half (warp >> 2) of the 64 key columns of each block.
+    // half (warp >> 2) of the 128 key columns of each block.
     const int quad = warp & 3;
     const int half = warp >> 2;
     const int r = quad * 32 + lane;
@@ -292,32 +326,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* rec = p.ld + (static_cast<int64_t>(h) * n_q64 + (qpos >> 6)) * 128;
     const float nlse2 = valid ? rec[qpos & 63] : 0.f;  // -LSE * log2(e)
     const float dlt = valid ? rec[64 + (qpos & 63)] : 0.f;
-    bool ok = warp_wait(bar(B_QDO_FULL), 0, w);
-    if (ok) {  // half 0 copies the Q row into TMEM, half 1 the dO row
-      tile_row_to_tmem(sb + (half == 0 ? OFF_Q : OFF_DO), r, trow + (half == 0 ? TM_Q : TM_DO));
-      tmem_st_wait();
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int b = j & 1;
+      if (!(ok = warp_wait(bar(B_S_FULL + b), (j >> 1) & 1, w))) break;
+      if (!(ok = warp_wait(bar(B_DP_FULL), j & 1, w))) break;
+      tc_fence_after();
+      const uint32_t ts = trow + TM_S + b * 128 + half * 64;
+      uint32_t s0[32], s1[32], d0[32], d1[32];
+      tmem_ld32(ts, s0);
+      tmem_ld32(ts + 32, s1);
+      tmem_ld32(trow + TM_DP + half * 64, d0);
+      tmem_ld32(trow + TM_DP + half * 64 + 32, d1);
+      tmem_ld_wait(s0);
+      tmem_ld_wait(s1);
+      tmem_ld_wait(d0);
+      tmem_ld_wait(d1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_QDO_TMEM));
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!(ok = warp_wait(bar(B_SDP_FULL + b), ph, w))) break;
-      tc_fence_after();
-      uint32_t sv[32], dv[32];
-      tmem_ld32(trow + TM_S + b * 64 + half * 32, sv);
-      tmem_ld32(trow + TM_DP + b * 64 + half * 32, dv);
-      tmem_ld_wait(sv);
-      tmem_ld_wait(dv);
-      const int k0 = j * 64 + half * 32;  // key of this warp's first column
-      uint32_t pk[16];
-      if (j >= 2 * qb)  // the diagonal tile (warp-uniform)
-        ds_slice<true>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
-      else
-        ds_slice<false>(sv, dv, sl2, nlse2, dlt, k0, qpos, pk);
-      // dS over the first 16 of the 32 S columns this warp just read.
-      tmem_st16(trow + TM_S + b * 64 + half * 32, pk);
+      if (lane == 0) mbar_arrive(bar(B_DP_EMPTY));
+      const int k0 = j * 128 + half * 64;  // key of this warp's first column
+      uint32_t pk0[16], pk1[16];
+      if (j == qb) {  // the diagonal block (warp-uniform)
+        ds_slice<true>(s0, d0, sl2, nlse2, dlt, k0, qpos, pk0);
+        ds_slice<true>(s1, d1, sl2, nlse2, dlt, k0 + 32, qpos, pk1);
+      } else {
+        ds_slice<false>(s0, d0, sl2, nlse2, dlt, k0, qpos, pk0);
+        ds_slice<false>(s1, d1, sl2, nlse2, dlt, k0 + 32, qpos, pk1);
+      }
+      // dS over the first 32 of the 64 S columns this warp just read.
+      tmem_st16(ts, pk0);
+      tmem_st16(ts + 16, pk1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -704,13 +743,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k64, const CUtensorMap& v64,
+cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const AttnBwdParams& p, int n_qblocks, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(n_qblocks, p.nheads);
-  attn_bwd_dq_kernel<<<grid, kThreads, dq::kSmemBytes, s>>>(q, k64, v64, dO, p);
+  attn_bwd_dq_kernel<<<grid, kThreads, dq::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }
 

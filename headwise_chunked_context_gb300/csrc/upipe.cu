@@ -531,7 +531,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     b.rope = rope;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv64, m_qkv64, m_do, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(m_qkv64, m_qkv, m_qkv, m_do64, b, m_tiles, st));
 
     // dWqkv rows of the chunk: q slots always, k/v slots once complete.
@@ -653,13 +653,11 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
   const int64_t L = s.L;
   const int m_tiles = static_cast<int>((L + 127) / 128);
   const int64_t Hd = static_cast<int64_t>(s.H) * 128, Hkvd = static_cast<int64_t>(s.Hkv) * 128;
-  CUtensorMap mq, mq64, mk, mv, mk64, mv64, mdo, mdo64;
+  CUtensorMap mq, mq64, mk, mv, mdo, mdo64;
   UPIPE_MAP(map3d(&mq, q, L, s.H, Hd, 128, 128));
   UPIPE_MAP(map3d(&mq64, q, L, s.H, Hd, 128, 64));
   UPIPE_MAP(map3d(&mk, k, L, s.Hkv, Hkvd, 128, 128));
   UPIPE_MAP(map3d(&mv, v, L, s.Hkv, Hkvd, 128, 128));
-  UPIPE_MAP(map3d(&mk64, k, L, s.Hkv, Hkvd, 128, 64));
-  UPIPE_MAP(map3d(&mv64, v, L, s.Hkv, Hkvd, 128, 64));
   UPIPE_MAP(map3d(&mdo, dout_o, L, s.H, Hd, 128, 128));
   UPIPE_MAP(map3d(&mdo64, dout_o, L, s.H, Hd, 128, 64));
   const int chunks_per_group = s.U < s.g ? s.g / s.U : 1;
@@ -695,7 +693,7 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.rope = nullptr;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk64, mv64, mdo, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk, mv, mdo, b, m_tiles, st));
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(mq64, mk, mv, mdo64, b, m_tiles, st));
   }
   return UPIPE_OK;

@@ -106,8 +106,8 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& 
                         cudaStream_t s);
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const AttnFwdParams& p, int n_qblocks, cudaStream_t s);
-// q, dO: 128-row boxes; k64, v64: 64-row boxes.
-cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k64, const CUtensorMap& v64,
+// All four maps with 128-row boxes.
+cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const AttnBwdParams& p, int n_qblocks, cudaStream_t s);
 cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dO64, const AttnBwdParams& p, int n_kblocks, cudaStream_t s);
