@@ -14,14 +14,16 @@
 //  * dq kernel: one CTA per (query head, 128-query tile) walks its 128-key
 //    blocks in ascending order and accumulates dQ in TMEM;
 //  * dkdv kernel: one CTA per (KV head, 128-key tile) walks the query heads
-//    that read this KV head (ascending) and, for each, the 64-query tiles at
-//    or after the key tile (ascending), accumulating dK and dV in TMEM.  When
+//    that read this KV head (ascending) and, for each, the 128-query tiles
+//    at or after the key tile (ascending), accumulating dK and dV in TMEM.  When
 //    a chunk holds fewer query heads than a KV group (U < g) the partial sums
 //    are carried in fp32 between chunks and reloaded into TMEM, which keeps
 //    the same order as a single pass over the whole group.
 //
 // Both kernels: warp 8 loads tiles with TMA (the dkdv producer also copies
-// the query tile's LSE/Delta record), warp 9 issues tcgen05.mma, and warps 0-7
+// the query tile's LSE/Delta records), warp 9 issues the products of
+// shared-memory operands (S, dP), warp 10 the products that read the
+// softmax tiles from TMEM (dQ, dV, dK), and warps 0-7
 // turn scores into P / dS: two warps share each TMEM lane quadrant and split
 // the columns, so every SM sub-partition has two of them to hide latency.
 // The tensor core reads shared-memory operands at about 128 B/clk per SM, so
@@ -33,9 +35,13 @@ namespace upipe {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634074f;
-constexpr int kThreads = 320;  // 8 compute warps, 1 producer warp, 1 MMA warp
+// 8 compute warps, 1 producer warp and 2 MMA-issuing warps: one thread
+// issues a tcgen05.mma about every 100 cycles at best, so two threads, each
+// owning its own accumulators, keep the tensor core busy.
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // products from shared-memory operands (S, dP)
+constexpr int kGradWarp = 10;  // products that consume the softmax tiles from TMEM
 constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
@@ -63,36 +69,51 @@ __device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// P^T and dS^T row slice of the dkdv kernel: 32 queries of one key row,
-// paired fp32 math.  kMask zeroes queries before the key (first two tiles).
+// P^T row slice of the dkdv kernel: 32 queries of one key row, kept in fp32
+// for the dS^T phase.  rec holds the queries' -LSE * log2(e); kMask zeroes
+// queries before the key (the diagonal tile only).
 template <bool kMask>
-__device__ __forceinline__ void pds_slice(const uint32_t (&sv)[32], const uint32_t (&dv)[32], const float4* l4,
-                                          const float4* d4, float sl2, int q0, int kpos, uint32_t (&pp)[16],
-                                          uint32_t (&dd)[16]) {
+__device__ __forceinline__ void p_slice(const uint32_t (&sv)[32], const float* rec, float sl2, int q0, int kpos,
+                                        float* pf) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const float4* l4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
   for (int c4 = 0; c4 < 8; ++c4) {
-    const float4 lv = l4[c4];  // -LSE * log2(e)
-    const float4 dl = d4[c4];  // Delta
+    const float4 lv = l4[c4];
+    float t0, t1, t2, t3;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), sl2x2,
+                     f2_pack(lv.x, lv.y)),
+              t0, t1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), sl2x2,
+                     f2_pack(lv.z, lv.w)),
+              t2, t3);
+    float p[4] = {ex2_approx(t0), ex2_approx(t1), ex2_approx(t2), ex2_approx(t3)};
 #pragma unroll
-    for (int e = 0; e < 4; e += 2) {
-      const int cc = c4 * 4 + e;
-      const float la0 = e == 0 ? lv.x : lv.z, la1 = e == 0 ? lv.y : lv.w;
-      const float da0 = e == 0 ? dl.x : dl.z, da1 = e == 0 ? dl.y : dl.w;
-      float t0, t1;
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[cc]), __uint_as_float(sv[cc + 1])), sl2x2, f2_pack(la0, la1)), t0,
-                t1);
-      float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-      if (kMask) {
-        if (q0 + cc < kpos) p0 = 0.f;
-        if (q0 + cc + 1 < kpos) p1 = 0.f;
-      }
-      const uint64_t d = f2_sub(f2_pack(__uint_as_float(dv[cc]), __uint_as_float(dv[cc + 1])), f2_pack(da0, da1));
-      float s0, s1;
-      f2_unpack(f2_mul(f2_pack(p0, p1), d), s0, s1);
-      pp[cc >> 1] = pack_bf16x2(p0, p1);
-      dd[cc >> 1] = pack_bf16x2(s0, s1);
+    for (int e = 0; e < 4; ++e) {
+      if (kMask && q0 + 4 * c4 + e < kpos) p[e] = 0.f;
+      pf[4 * c4 + e] = p[e];
     }
+  }
+}
+
+// dS^T row slice of the dkdv kernel: dS = P * (dP - Delta) for 32 queries,
+// packed bf16.  rec holds the queries' Delta.
+__device__ __forceinline__ void dst_slice(const uint32_t (&dv)[32], const float* pf, const float* rec,
+                                          uint32_t (&dd)[16]) {
+  const float4* d4 = reinterpret_cast<const float4*>(rec);
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const float4 dl = d4[c4];
+    float s0, s1, s2, s3;
+    f2_unpack(f2_mul(f2_pack(pf[4 * c4], pf[4 * c4 + 1]),
+                     f2_sub(f2_pack(__uint_as_float(dv[4 * c4]), __uint_as_float(dv[4 * c4 + 1])), f2_pack(dl.x, dl.y))),
+              s0, s1);
+    f2_unpack(f2_mul(f2_pack(pf[4 * c4 + 2], pf[4 * c4 + 3]),
+                     f2_sub(f2_pack(__uint_as_float(dv[4 * c4 + 2]), __uint_as_float(dv[4 * c4 + 3])),
+                            f2_pack(dl.z, dl.w))),
+              s2, s3);
+    dd[2 * c4] = pack_bf16x2(s0, s1);
+    dd[2 * c4 + 1] = pack_bf16x2(s2, s3);
   }
 }
 
@@ -127,6 +148,7 @@ enum {
   B_DP_EMPTY,                // the compute warps have read dP
   B_DQ_DONE,
   B_DRAIN,
+  B_DRAIN_G,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
@@ -171,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DP_EMPTY), kComputeWarps);
     mbar_init(bar(B_DQ_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN_G), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -235,10 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
-      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);   // dQ += dS K (dS from TMEM, K MN-major)
-      // Event-driven issue of three product kinds: S(ns) once K(ns) has
-      // landed and dQ(ns - 2) has released the buffer; dP(nd) once V(nd) has
-      // landed and dP(nd - 1) has been read; dQ(nq) once dS(nq) is written.
+      // Event-driven issue of S(ns) once K(ns) has landed and dQ(ns - 2) has
+      // released the buffer, and dP(nd) once V(nd) has landed and dP(nd - 1)
+      // has been read.
       auto s_ready = [&](int j) {
         return mbar_test(bar(B_K_FULL + j % kStages), (j / kStages) & 1) &&
                mbar_test(bar(B_S_FREE + (j & 1)), ((j >> 1) & 1) ^ 1);
@@ -247,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         return mbar_test(bar(B_V_FULL + j % kStages), (j / kStages) & 1) &&
                mbar_test(bar(B_DP_EMPTY), (j & 1) ^ 1);
       };
-      auto dq_ready = [&](int j) { return mbar_test(bar(B_DS_FULL + (j & 1)), (j >> 1) & 1); };
       auto issue_s = [&](int j) {
         const uint32_t ka = sb + OFF_K + (j % kStages) * kTile;
 #pragma unroll
@@ -270,25 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bar(B_DP_FULL));
         umma_commit(bar(B_V_EMPTY + s));
       };
-      auto issue_dq = [&](int j) {
-        const int b = j & 1;
-        const int s = j % kStages;
-        const uint32_t ka = sb + OFF_K + s * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // keys 16 kk .. 16 kk + 15: compute half kk / 4 wrote them at its own
-          // 64-column slice of the S buffer
-          const uint32_t a = tmem + TM_S + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_bf16_ts(tmem + TM_DQ, a, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_S_FREE + b));
-        umma_commit(bar(B_K_EMPTY + s));
-      };
       bool ok = mbar_wait(bar(B_QDO_FULL), 0, w);
-      int ns = 0, nd = 0, nq = 0;
+      int ns = 0, nd = 0;
       Watchdog wd;
       wd.reset();
-      while (ok && nq < n_kv) {
+      while (ok && nd < n_kv) {
         bool did = false;
         if (ns < n_kv && ns <= nd + 1 && s_ready(ns)) {
           tc_fence_after();
@@ -300,17 +307,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(nd++);
           did = true;
         }
-        if (nq < nd && dq_ready(nq)) {
-          tc_fence_after();
-          issue_dq(nq++);
-          did = true;
-        }
         if (did) wd.reset();
         else ok = wd.alive(w);
       }
-      if (ok) umma_commit(bar(B_DQ_DONE));
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
+    }
+  } else if (warp == kGradWarp) {
+    if (lane == 0) {
+      // dQ(j) += dS(j) K(j) once dS(j) is written; then S buffer j & 1 and
+      // K stage j % kStages are free (S(j) had completed before dS(j) existed).
+      constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dS from TMEM, K MN-major
+      bool ok = true;
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int b = j & 1;
+        const int s = j % kStages;
+        if (!(ok = mbar_spin(bar(B_DS_FULL + b), (j >> 1) & 1, w))) break;
+        tc_fence_after();
+        const uint32_t ka = sb + OFF_K + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // keys 16 kk .. 16 kk + 15: compute half kk / 4 wrote them at its own
+          // 64-column slice of the S buffer
+          const uint32_t a = tmem + TM_S + b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_bf16_ts(tmem + TM_DQ, a, sdesc_sw128(ka + kk * 2048, kHalf, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_S_FREE + b));
+        umma_commit(bar(B_K_EMPTY + s));
+      }
+      if (ok) umma_commit(bar(B_DQ_DONE));
+      umma_commit(bar(B_DRAIN_G));
+      mbar_wait_drain(bar(B_DRAIN_G), 0, p.status);
     }
   } else {
     // Compute warps: quadrant (warp & 3) of the TMEM lanes = query rows,
@@ -407,33 +434,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ============================================================ dK/dV kernel
 //
-// S^T and dP^T of a 64-query tile live in TMEM buffer it & 1; the compute
-// warps write P^T and dS^T (packed bf16) over the columns they have read,
-// and dV += P^T dO, dK += dS^T Q take them straight from TMEM.  Q/dO tiles
-// and their LSE/Delta records stream through a 4-stage ring.
+// 128-query tiles, so every product is an M=128, N=128 tcgen05.mma.  TMEM
+// holds S^T (128 columns), dP^T (128), dV and dK; with no room for a second
+// S^T/dP^T buffer the compute warps work in two phases per tile: P^T as soon
+// as S^T has landed (written packed over the S^T columns they read, feeding
+// dV while dP^T is still being formed), then dS^T = P^T * (dP^T - Delta)
+// over the dP^T columns (feeding dK).  S^T of the next tile is issued as soon
+// as dV has consumed P^T, ahead of dK when dS^T is not yet written, so the
+// tensor pipe works on it while the compute warps finish dS^T.
+// Q/dO tiles and their two LSE/Delta records stream through a 2-stage ring.
 
 namespace dkv {
-constexpr int kKV = 128 * 128 * 2;  // K or V tile: [128 keys][128 d]
-constexpr int kKVHalf = kKV / 2;
-constexpr int kQ = 64 * 128 * 2;    // Q or dO tile: [64 queries][128 d]
-constexpr int kQHalf = kQ / 2;
-constexpr int kStages = 4;          // Q/dO ring depth
+constexpr int kTile = 128 * 128 * 2;  // K, V, Q or dO tile: [128 rows][128 d]
+constexpr int kHalf = kTile / 2;
+constexpr int kStages = 2;            // Q/dO ring depth
+constexpr int kRec = 512;             // one 64-query LSE/Delta record
 constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + kKV;
-constexpr int OFF_Q = OFF_V + kKV;             // kStages stages
-constexpr int OFF_DO = OFF_Q + kStages * kQ;
-constexpr int OFF_LD = OFF_DO + kStages * kQ;  // per stage: the tile's LSE/Delta record
-constexpr int OFF_BAR = OFF_LD + kStages * 512;
+constexpr int OFF_V = OFF_K + kTile;
+constexpr int OFF_Q = OFF_V + kTile;             // kStages stages
+constexpr int OFF_DO = OFF_Q + kStages * kTile;
+constexpr int OFF_LD = OFF_DO + kStages * kTile;  // per stage: two records
+constexpr int OFF_BAR = OFF_LD + kStages * 2 * kRec;
 enum {
   B_KV_FULL,
   B_QDO_FULL,
   B_QDO_EMPTY = B_QDO_FULL + kStages,
-  B_SDP_FULL = B_QDO_EMPTY + kStages,
-  B_PDS_FULL = B_SDP_FULL + 2,
-  B_SDP_FREE = B_PDS_FULL + 2,  // dV/dK of that buffer done: S^T/P^T and dP^T/dS^T columns free
-  B_CARRY_READY = B_SDP_FREE + 2,
+  B_S_FULL = B_QDO_EMPTY + kStages,
+  B_DP_FULL,
+  B_P_FULL,    // P^T written (compute warps)
+  B_DS_FULL,   // dS^T written (compute warps)
+  B_S_FREE,    // dV done: S^T / P^T columns free
+  B_DP_FREE,   // dK done: dP^T / dS^T columns free
+  B_CARRY_READY,
   B_DKV_DONE,
   B_DRAIN,
+  B_DRAIN_G,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
@@ -455,13 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = blockIdx.x;  // key tile 0 sees every query: the heaviest tiles launch first
   const int kv = blockIdx.y;
   const int n_q64 = (p.L + 63) / 64;
-  const int nqi = n_q64 - 2 * kb;  // query tiles at or after this key tile
-  const int n_it = p.g_loc * nqi;
+  const int n_q128 = (p.L + 127) / 128;
+  const int nqt = n_q128 - kb;  // query tiles at or after this key tile
+  const int n_it = p.g_loc * nqt;
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
   const bool carry_in = p.carry_in != 0;
-  float* ld_smem = reinterpret_cast<float*>(smem + OFF_LD);
+  const float* ld_smem = reinterpret_cast<const float*>(smem + OFF_LD);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV_FULL), 1);
@@ -469,14 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_QDO_FULL + s), 1);
       mbar_init(bar(B_QDO_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_SDP_FULL + b), 1);
-      mbar_init(bar(B_PDS_FULL + b), kComputeWarps);
-      mbar_init(bar(B_SDP_FREE + b), 1);
-    }
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_DP_FULL), 1);
+    mbar_init(bar(B_P_FULL), kComputeWarps);
+    mbar_init(bar(B_DS_FULL), kComputeWarps);
+    mbar_init(bar(B_S_FREE), 1);
+    mbar_init(bar(B_DP_FREE), 1);
     mbar_init(bar(B_CARRY_READY), kComputeWarps);
     mbar_init(bar(B_DKV_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN_G), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -490,8 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
 
   if (warp == kProducerWarp) {
-    // Q and dO tiles (TMA) plus the tile's LSE/Delta record (bulk copy), all
-    // on one barrier per stage.
+    // Q and dO tiles (TMA) plus the tile's LSE/Delta records (bulk copy; the
+    // second is absent when the tile's upper 64 queries lie past L), all on
+    // one barrier per stage.
     if (lane == 0) {
       int last[kStages];
 #pragma unroll
@@ -500,23 +539,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&mk);
       tma_prefetch_map(&mv);
       tma_prefetch_map(&mdo);
-      mbar_expect_tx(bar(B_KV_FULL), 2 * kKV);
+      mbar_expect_tx(bar(B_KV_FULL), 2 * kTile);
       tma_load_3d(sb + OFF_K, &mk, bar(B_KV_FULL), 0, kb * 128, p.k_z0 + kv);
-      tma_load_3d(sb + OFF_K + kKVHalf, &mk, bar(B_KV_FULL), 64, kb * 128, p.k_z0 + kv);
+      tma_load_3d(sb + OFF_K + kHalf, &mk, bar(B_KV_FULL), 64, kb * 128, p.k_z0 + kv);
       tma_load_3d(sb + OFF_V, &mv, bar(B_KV_FULL), 0, kb * 128, p.v_z0 + kv);
-      tma_load_3d(sb + OFF_V + kKVHalf, &mv, bar(B_KV_FULL), 64, kb * 128, p.v_z0 + kv);
+      tma_load_3d(sb + OFF_V + kHalf, &mv, bar(B_KV_FULL), 64, kb * 128, p.v_z0 + kv);
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const int hl = kv * p.g_loc + it / nqi;
-        const int qi = 2 * kb + it % nqi;
+        const int hl = kv * p.g_loc + it / nqt;
+        const int qt = kb + it % nqt;
+        const int recs = 2 * qt + 1 < n_q64 ? 2 : 1;
         if (!mbar_wait(bar(B_QDO_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kQ + 512);
-        tma_load_3d(sb + OFF_Q + s * kQ, &mq, bar(B_QDO_FULL + s), 0, qi * 64, p.q_z0 + hl);
-        tma_load_3d(sb + OFF_Q + s * kQ + kQHalf, &mq, bar(B_QDO_FULL + s), 64, qi * 64, p.q_z0 + hl);
-        tma_load_3d(sb + OFF_DO + s * kQ, &mdo, bar(B_QDO_FULL + s), 0, qi * 64, p.do_z0 + hl);
-        tma_load_3d(sb + OFF_DO + s * kQ + kQHalf, &mdo, bar(B_QDO_FULL + s), 64, qi * 64, p.do_z0 + hl);
-        bulk_load(sb + OFF_LD + s * 512, p.ld + (static_cast<int64_t>(hl) * n_q64 + qi) * 128, 512,
+        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kTile + recs * kRec);
+        tma_load_3d(sb + OFF_Q + s * kTile, &mq, bar(B_QDO_FULL + s), 0, qt * 128, p.q_z0 + hl);
+        tma_load_3d(sb + OFF_Q + s * kTile + kHalf, &mq, bar(B_QDO_FULL + s), 64, qt * 128, p.q_z0 + hl);
+        tma_load_3d(sb + OFF_DO + s * kTile, &mdo, bar(B_QDO_FULL + s), 0, qt * 128, p.do_z0 + hl);
+        tma_load_3d(sb + OFF_DO + s * kTile + kHalf, &mdo, bar(B_QDO_FULL + s), 64, qt * 128, p.do_z0 + hl);
+        bulk_load(sb + OFF_LD + s * 2 * kRec, p.ld + (static_cast<int64_t>(hl) * n_q64 + 2 * qt) * 128, recs * kRec,
                   bar(B_QDO_FULL + s));
         last[s] = it;
       }
@@ -528,85 +568,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
-      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // dV += P^T dO, dK += dS^T Q (A from TMEM)
-      // Event-driven issue: S^T/dP^T of tile ns once its Q/dO stage has
-      // landed and the dV/dK products of tile ns - 2 (which read the same
-      // TMEM buffers) are done; dV/dK of tile ng once P^T/dS^T are written.
-      auto sdp_ready = [&](int it) {
-        return mbar_test(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1) &&
-               mbar_test(bar(B_SDP_FREE + (it & 1)), ((it >> 1) & 1) ^ 1);
-      };
-      auto grad_ready = [&](int it) { return mbar_test(bar(B_PDS_FULL + (it & 1)), (it >> 1) & 1); };
-      auto issue_sdp = [&](int it) {
-        const int b = it & 1;
-        const int qs = it % kStages;
-        const uint32_t qa = sb + OFF_Q + qs * kQ;
-        const uint32_t da = sb + OFF_DO + qs * kQ;
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+      // Event-driven issue: S^T(i) once its Q/dO stage has landed and dV(i - 1)
+      // is done; dP^T(i) once dK(i - 1) is done.
+      auto qdo_full = [&](int it) { return mbar_test(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1); };
+      auto s_ready = [&](int it) { return qdo_full(it) && mbar_test(bar(B_S_FREE), (it & 1) ^ 1); };
+      auto dp_ready = [&](int it) { return qdo_full(it) && mbar_test(bar(B_DP_FREE), (it & 1) ^ 1); };
+      auto issue_kq = [&](int it, uint32_t a_base, uint32_t b_base, int tm, int done) {
+        const uint32_t bq = b_base + (it % kStages) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-          const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_ST + b * 64, sdesc_sw128(sb + OFF_K + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024),
-                    id_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024), id_s,
+                    kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-          const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          umma_bf16(tmem + TM_DPT + b * 64, sdesc_sw128(sb + OFF_V + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024),
-                    id_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(B_SDP_FULL + b));
-      };
-      auto issue_grad = [&](int it) {
-        const int b = it & 1;
-        const int qs = it % kStages;
-        const uint32_t qa = sb + OFF_Q + qs * kQ;
-        const uint32_t da = sb + OFF_DO + qs * kQ;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // queries 16 kk .. 16 kk + 15: written by compute half kk / 2
-          const uint32_t col = b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + TM_DV, tmem + TM_ST + col, sdesc_sw128(da + kk * 2048, kQHalf, 1024), id_g,
-                       (carry_in || it > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t col = b * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_ts(tmem + TM_DK, tmem + TM_DPT + col, sdesc_sw128(qa + kk * 2048, kQHalf, 1024), id_g,
-                       (carry_in || it > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_SDP_FREE + b));
-        umma_commit(bar(B_QDO_EMPTY + qs));
+        umma_commit(bar(done));
       };
       bool ok = mbar_wait(bar(B_KV_FULL), 0, w);
-      if (ok && carry_in) ok = mbar_wait(bar(B_CARRY_READY), 0, w);
-      int ns = 0, ng = 0;
+      int ns = 0, nd = 0;
       Watchdog wd;
       wd.reset();
-      while (ok && ng < n_it) {
+      while (ok && nd < n_it) {
         bool did = false;
-        if (ns < n_it && sdp_ready(ns)) {
+        if (ns < n_it && s_ready(ns)) {
           tc_fence_after();
-          issue_sdp(ns++);
+          issue_kq(ns, sb + OFF_K, sb + OFF_Q, TM_ST, B_S_FULL);
+          ++ns;
           did = true;
         }
-        if (ng < ns && grad_ready(ng)) {
+        if (nd < ns && dp_ready(nd)) {
           tc_fence_after();
-          issue_grad(ng++);
+          issue_kq(nd, sb + OFF_V, sb + OFF_DO, TM_DPT, B_DP_FULL);
+          ++nd;
           did = true;
         }
         if (did) wd.reset();
         else ok = wd.alive(w);
       }
-      if (ok) umma_commit(bar(B_DKV_DONE));
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
+  } else if (warp == kGradWarp) {
+    if (lane == 0) {
+      // dV(i) += P^T(i) dO(i) once P^T is written (then the S^T columns are
+      // free), dK(i) += dS^T(i) Q(i) once dS^T is written (then the dP^T
+      // columns and the Q/dO stage are free: S^T(i) and dP^T(i) had completed
+      // before the compute warps could write P^T and dS^T).
+      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // A from TMEM, B MN-major
+      auto issue_grad = [&](int it, int tm_a, uint32_t b_base, int tm_d) {
+        const uint32_t bq = b_base + (it % kStages) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // queries 16 kk .. 16 kk + 15: compute half kk / 4 wrote them at
+          // its own 64-column slice
+          const uint32_t a = tmem + tm_a + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_bf16_ts(tmem + tm_d, a, sdesc_sw128(bq + kk * 2048, kHalf, 1024), id_g,
+                       (carry_in || it > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      if (carry_in) ok = mbar_wait(bar(B_CARRY_READY), 0, w);
+      for (int it = 0; ok && it < n_it; ++it) {
+        if (!(ok = mbar_spin(bar(B_P_FULL), it & 1, w))) break;
+        tc_fence_after();
+        issue_grad(it, TM_ST, sb + OFF_DO, TM_DV);
+        umma_commit(bar(B_S_FREE));
+        if (!(ok = mbar_spin(bar(B_DS_FULL), it & 1, w))) break;
+        // S^T of the next tile is on the critical path (P^T, then dV, wait
+        // for it); dK only gates dP^T of the next tile, which is needed later.
+        // So dK waits until S^T(it + 1) has landed rather than share the
+        // tensor pipe with it.
+        if (it + 1 < n_it && !(ok = mbar_spin(bar(B_S_FULL), (it + 1) & 1, w))) break;
+        tc_fence_after();
+        issue_grad(it, TM_DPT, sb + OFF_Q, TM_DK);
+        umma_commit(bar(B_DP_FREE));
+        umma_commit(bar(B_QDO_EMPTY + it % kStages));
+      }
+      if (ok) umma_commit(bar(B_DKV_DONE));
+      umma_commit(bar(B_DRAIN_G));
+      mbar_wait_drain(bar(B_DRAIN_G), 0, p.status);
+    }
   } else {
     // Compute warps: quadrant (warp & 3) of the key rows, half (warp >> 2) of
-    // the 64 query columns of each tile.
+    // the 128 query columns of each tile.
     const int quad = warp & 3;
     const int half = warp >> 2;
     const int r = quad * 32 + lane;  // key row = TMEM lane
@@ -637,34 +681,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_CARRY_READY));
     }
+    const uint32_t ts = trow + TM_ST + half * 64;
+    const uint32_t td = trow + TM_DPT + half * 64;
     for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
       const int qs = it % kStages;
-      const int qi = 2 * kb + it % nqi;
-      if (!(ok = warp_wait(bar(B_SDP_FULL + b), ph, w))) break;
-      tc_fence_after();
-      uint32_t sv[32], dv[32];
-      tmem_ld32(trow + TM_ST + b * 64 + half * 32, sv);
-      tmem_ld32(trow + TM_DPT + b * 64 + half * 32, dv);
-      tmem_ld_wait(sv);
-      tmem_ld_wait(dv);
+      const int qt = kb + it % nqt;
+      const int q0 = qt * 128 + half * 64;  // query of this warp's first column
+      // Without its record (all 64 queries past L) the slice is all zero.
+      const bool live = 2 * qt + half < n_q64;
+      const float* rec = ld_smem + qs * 256 + half * 128;
+      // ---- phase 1: P^T over the S^T columns
+      if (!(ok = warp_wait(bar(B_S_FULL), it & 1, w))) break;
       if (!(ok = warp_wait(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
-      const float4* l4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + half * 32);
-      const float4* d4 = reinterpret_cast<const float4*>(ld_smem + qs * 128 + 64 + half * 32);
-      const int q0 = qi * 64 + half * 32;
-      uint32_t pp[16], dd[16];
-      if (qi < 2 * kb + 2)  // query tiles overlapping the key tile (warp-uniform)
-        pds_slice<true>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
-      else
-        pds_slice<false>(sv, dv, l4, d4, sl2, q0, kpos, pp, dd);
-      // P^T and dS^T over the first 16 of the 32 columns this warp just read.
-      tmem_st16(trow + TM_ST + b * 64 + half * 32, pp);
-      tmem_st16(trow + TM_DPT + b * 64 + half * 32, dd);
-      tmem_st_wait();
+      tc_fence_after();
+      float pf[64];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld32(ts, s0);
+        tmem_ld32(ts + 32, s1);
+        tmem_ld_wait(s0);
+        tmem_ld_wait(s1);
+        uint32_t pk0[16], pk1[16];
+        if (!live) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pf[c] = 0.f;
+        } else if (qt == kb) {  // the diagonal tile (warp-uniform)
+          p_slice<true>(s0, rec, sl2, q0, kpos, pf);
+          p_slice<true>(s1, rec + 32, sl2, q0 + 32, kpos, pf + 32);
+        } else {
+          p_slice<false>(s0, rec, sl2, q0, kpos, pf);
+          p_slice<false>(s1, rec + 32, sl2, q0 + 32, kpos, pf + 32);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          pk0[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
+          pk1[c] = pack_bf16x2(pf[32 + 2 * c], pf[32 + 2 * c + 1]);
+        }
+        tmem_st16(ts, pk0);
+        tmem_st16(ts + 16, pk1);
+        tmem_st_wait();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PDS_FULL + b));
+      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      // ---- phase 2: dS^T = P^T * (dP^T - Delta) over the dP^T columns
+      if (!(ok = warp_wait(bar(B_DP_FULL), it & 1, w))) break;
+      tc_fence_after();
+      {
+        uint32_t d0[32], d1[32];
+        tmem_ld32(td, d0);
+        tmem_ld32(td + 32, d1);
+        tmem_ld_wait(d0);
+        tmem_ld_wait(d1);
+        uint32_t dd0[16], dd1[16];
+        if (!live) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dd0[c] = dd1[c] = 0u;
+        } else {
+          dst_slice(d0, pf, rec + 64, dd0);
+          dst_slice(d1, pf + 32, rec + 96, dd1);
+        }
+        tmem_st16(td, dd0);
+        tmem_st16(td + 16, dd1);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DS_FULL));
     }
     if (ok) ok = warp_wait(bar(B_DKV_DONE), 0, w);
     if (ok) {
@@ -753,13 +836,13 @@ cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& dO64, const AttnBwdParams& p, int n_kblocks, cudaStream_t s) {
+cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dO, const AttnBwdParams& p, int n_kblocks, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(n_kblocks, p.nkv);
-  attn_bwd_dkdv_kernel<<<grid, kThreads, dkv::kSmemBytes, s>>>(q64, k, v, dO64, p);
+  attn_bwd_dkdv_kernel<<<grid, kThreads, dkv::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }
 

@@ -104,6 +104,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Bounded wait that spins on the non-blocking probe instead of try_wait, for
+// a thread whose next action is latency-critical (an MMA issuer): no
+// suspend/wake-up between the phase completing and the thread noticing.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 31) != 0) continue;  // the abort flag and the clock every 32 polls
+    if (*w.abort_flag) return false;
+    const uint64_t now = global_timer_ns();
+    if (i == 32) {
+      t0 = now;
+    } else if (now - t0 > w.limit_ns) {
+      *w.abort_flag = 1;
+      atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Drain wait used while unwinding: ignores the abort flag, bounded by a fixed
 // limit.  Used only on events that complete without help from other threads
 // (TMA bytes landing, issued MMAs retiring).
@@ -124,22 +144,29 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // all 32 lanes; the result is warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_spin(bar, parity, w) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) mbar_try_wait(bar, parity);
   return ok != 0;
 }
 
 // No-progress watchdog for a thread that polls several barriers with
-// non-blocking try_wait and issues whatever is ready: `alive` turns false
+// non-blocking probes and issues whatever is ready: `alive` turns false
 // (raising the abort flag and the timeout status) once `limit_ns` passes
-// without progress, or as soon as another thread of the CTA aborted.
+// without progress, or as soon as another thread of the CTA aborted.  The
+// clock (a slow special-register read) is sampled only every 32 idle polls,
+// so that a poll that finds work ready reacts within a few cycles.
 struct Watchdog {
   uint64_t t0;
-  __device__ __forceinline__ void reset() { t0 = global_timer_ns(); }
+  uint32_t idle;
+  __device__ __forceinline__ void reset() { idle = 0; }
   __device__ __forceinline__ bool alive(const WaitCtl& w) {
+    if ((++idle & 31) != 0) return true;  // the abort flag and the clock every 32 idle polls
     if (*w.abort_flag) return false;
-    if (global_timer_ns() - t0 > w.limit_ns) {
+    const uint64_t now = global_timer_ns();
+    if (idle == 32) {
+      t0 = now;
+    } else if (now - t0 > w.limit_ns) {
       *w.abort_flag = 1;
       atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
       return false;

@@ -411,20 +411,18 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
 
   const bf16* obuf = o_saved ? reinterpret_cast<const bf16*>(o_saved) : reinterpret_cast<bf16*>(w + pl.off_o);
   const int64_t ld_o = o_saved ? Hd : static_cast<int64_t>(s.U) * 128;
-  CUtensorMap m_x, m_xmn, m_wqkv, m_wqkv_mn, m_qkv, m_qkv64, m_wo_mn, m_dout, m_dout_mn, m_o_mn, m_do, m_do64,
+  CUtensorMap m_x, m_xmn, m_wqkv, m_wqkv_mn, m_qkv, m_wo_mn, m_dout, m_dout_mn, m_o_mn, m_do,
       m_dqkv_k, m_dqkv_mn;
   UPIPE_MAP(map2d(&m_x, x, s.D, L, s.D, 128));
   UPIPE_MAP(map2d(&m_xmn, x, s.D, L, s.D, 64));
   UPIPE_MAP(map2d(&m_wqkv, Wqkv, s.D, static_cast<uint64_t>(s.H + 2 * s.Hkv) * 128, s.D, 128));
   UPIPE_MAP(map2d(&m_wqkv_mn, Wqkv, s.D, static_cast<uint64_t>(s.H + 2 * s.Hkv) * 128, s.D, 64));
   UPIPE_MAP(map3d(&m_qkv, qkv, L, slots, 128, L * 128, 128));
-  UPIPE_MAP(map3d(&m_qkv64, qkv, L, slots, 128, L * 128, 64));
   UPIPE_MAP(map2d(&m_wo_mn, Wo, Hd, s.D, Hd, 64));
   UPIPE_MAP(map2d(&m_dout, dout, s.D, L, s.D, 128));
   UPIPE_MAP(map2d(&m_dout_mn, dout, s.D, L, s.D, 64));
   UPIPE_MAP(map2d(&m_o_mn, obuf, ld_o, L, ld_o, 64));
   UPIPE_MAP(map3d(&m_do, dO, L, s.U, 128, L * 128, 128));
-  UPIPE_MAP(map3d(&m_do64, dO, L, s.U, 128, L * 128, 64));
   UPIPE_MAP(map3d(&m_dqkv_k, dqkv, L, 2 * slots, 128, L * 128, 128));
   UPIPE_MAP(map3d(&m_dqkv_mn, dqkv, L, 2 * slots, 128, L * 128, 64));
 
@@ -532,7 +530,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     b.status = status;
     b.limit_ns = limit;
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(m_qkv64, m_qkv, m_qkv, m_do64, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
 
     // dWqkv rows of the chunk: q slots always, k/v slots once complete.
     const int out_slots = emit_kv ? slots : s.U;
@@ -653,13 +651,11 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
   const int64_t L = s.L;
   const int m_tiles = static_cast<int>((L + 127) / 128);
   const int64_t Hd = static_cast<int64_t>(s.H) * 128, Hkvd = static_cast<int64_t>(s.Hkv) * 128;
-  CUtensorMap mq, mq64, mk, mv, mdo, mdo64;
+  CUtensorMap mq, mk, mv, mdo;
   UPIPE_MAP(map3d(&mq, q, L, s.H, Hd, 128, 128));
-  UPIPE_MAP(map3d(&mq64, q, L, s.H, Hd, 128, 64));
   UPIPE_MAP(map3d(&mk, k, L, s.Hkv, Hkvd, 128, 128));
   UPIPE_MAP(map3d(&mv, v, L, s.Hkv, Hkvd, 128, 128));
   UPIPE_MAP(map3d(&mdo, dout_o, L, s.H, Hd, 128, 128));
-  UPIPE_MAP(map3d(&mdo64, dout_o, L, s.H, Hd, 128, 64));
   const int chunks_per_group = s.U < s.g ? s.g / s.U : 1;
   for (int c = 0; c < s.nch; ++c) {
     const Chunk ch = chunk_of(s, c);
@@ -694,7 +690,7 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.status = status;
     b.limit_ns = limit;
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk, mv, mdo, b, m_tiles, st));
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(mq64, mk, mv, mdo64, b, m_tiles, st));
+    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(mq, mk, mv, mdo, b, m_tiles, st));
   }
   return UPIPE_OK;
 }

@@ -106,11 +106,11 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& 
                         cudaStream_t s);
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const AttnFwdParams& p, int n_qblocks, cudaStream_t s);
-// All four maps with 128-row boxes.
+// All maps of the two backward kernels have 128-row boxes.
 cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dO, const AttnBwdParams& p, int n_qblocks, cudaStream_t s);
-cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& dO64, const AttnBwdParams& p, int n_kblocks, cudaStream_t s);
+cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dO, const AttnBwdParams& p, int n_kblocks, cudaStream_t s);
 cudaError_t launch_rope_table(float2* table, int64_t L, double theta, cudaStream_t s);
 // Writes the LSE/Delta records of AttnBwdParams::ld for `nheads` heads.
 cudaError_t launch_delta(const __nv_bfloat16* o, int64_t o_row, int64_t o_head, const __nv_bfloat16* dO,
