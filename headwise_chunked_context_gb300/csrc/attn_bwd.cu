@@ -34,7 +34,6 @@
 namespace upipe {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634074f;
 // 8 compute warps, 1 producer warp and 2 MMA-issuing warps: one thread
 // issues a tcgen05.mma about every 100 cycles at best, so two threads, each
 // owning its own accumulators, keep the tensor core busy.
@@ -69,16 +68,15 @@ __device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// P^T row slice of the dkdv kernel: 32 queries of one key row, kept in fp32
-// for the dS^T phase.  rec holds the queries' -LSE * log2(e); kMask zeroes
+// P^T row slice of the dkdv kernel: 16 queries of one key row, kept in fp32
+// for the dS^T phase.  l4 holds the queries' -LSE * log2(e); kMask zeroes
 // queries before the key (the diagonal tile only).
 template <bool kMask>
-__device__ __forceinline__ void p_slice(const uint32_t (&sv)[32], const float* rec, float sl2, int q0, int kpos,
+__device__ __forceinline__ void p_slice(const uint32_t (&sv)[16], const float4 (&l4)[4], float sl2, int q0, int kpos,
                                         float* pf) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
-  const float4* l4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
-  for (int c4 = 0; c4 < 8; ++c4) {
+  for (int c4 = 0; c4 < 4; ++c4) {
     const float4 lv = l4[c4];
     float t0, t1, t2, t3;
     f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), sl2x2,
@@ -96,13 +94,12 @@ __device__ __forceinline__ void p_slice(const uint32_t (&sv)[32], const float* r
   }
 }
 
-// dS^T row slice of the dkdv kernel: dS = P * (dP - Delta) for 32 queries,
-// packed bf16.  rec holds the queries' Delta.
-__device__ __forceinline__ void dst_slice(const uint32_t (&dv)[32], const float* pf, const float* rec,
-                                          uint32_t (&dd)[16]) {
-  const float4* d4 = reinterpret_cast<const float4*>(rec);
+// dS^T row slice of the dkdv kernel: dS = P * (dP - Delta) for 16 queries,
+// packed bf16.  d4 holds the queries' Delta.
+__device__ __forceinline__ void dst_slice(const uint32_t (&dv)[16], const float* pf, const float4 (&d4)[4],
+                                          uint32_t (&dd)[8]) {
 #pragma unroll
-  for (int c4 = 0; c4 < 8; ++c4) {
+  for (int c4 = 0; c4 < 4; ++c4) {
     const float4 dl = d4[c4];
     float s0, s1, s2, s3;
     f2_unpack(f2_mul(f2_pack(pf[4 * c4], pf[4 * c4 + 1]),
@@ -114,6 +111,15 @@ __device__ __forceinline__ void dst_slice(const uint32_t (&dv)[32], const float*
               s2, s3);
     dd[2 * c4] = pack_bf16x2(s0, s1);
     dd[2 * c4 + 1] = pack_bf16x2(s2, s3);
+  }
+}
+
+// Four float4 of a record (16 consecutive floats) from global memory.
+__device__ __forceinline__ void load_rec16(const float* p, bool live, float4 (&v)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 x = live ? ld_global_nc_v4(p + 4 * c) : make_uint4(0, 0, 0, 0);
+    v[c] = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w));
   }
 }
 
@@ -442,19 +448,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // over the dP^T columns (feeding dK).  S^T of the next tile is issued as soon
 // as dV has consumed P^T, ahead of dK when dS^T is not yet written, so the
 // tensor pipe works on it while the compute warps finish dS^T.
-// Q/dO tiles and their two LSE/Delta records stream through a 2-stage ring.
+// Q/dO tiles stream through a 2-stage TMA ring.  The compute warps read the
+// queries' LSE/Delta records straight from global memory (L1-cached, one
+// broadcast line per warp): kept out of shared memory, their loads and the
+// warps' barrier polls do not queue behind the ring's 64 KB TMA bursts.
 
 namespace dkv {
 constexpr int kTile = 128 * 128 * 2;  // K, V, Q or dO tile: [128 rows][128 d]
 constexpr int kHalf = kTile / 2;
 constexpr int kStages = 2;            // Q/dO ring depth
-constexpr int kRec = 512;             // one 64-query LSE/Delta record
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kTile;
 constexpr int OFF_Q = OFF_V + kTile;             // kStages stages
 constexpr int OFF_DO = OFF_Q + kStages * kTile;
-constexpr int OFF_LD = OFF_DO + kStages * kTile;  // per stage: two records
-constexpr int OFF_BAR = OFF_LD + kStages * 2 * kRec;
+constexpr int OFF_BAR = OFF_DO + kStages * kTile;
 enum {
   B_KV_FULL,
   B_QDO_FULL,
@@ -475,9 +482,17 @@ constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
 constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
 constexpr int TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = 384;
+// 16 compute warps: four per TMEM lane quadrant, each owning 32 of the 128
+// query columns, so each SM sub-partition has four to hide TMEM and exp2
+// latency; then the producer and the two MMA-issuing warps.
+constexpr int kCompute = 16;
+constexpr int kProducer = 16;
+constexpr int kMma = 17;
+constexpr int kGrad = 18;
+constexpr int kThreadsKv = 608;
 }  // namespace dkv
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dkv::kThreadsKv, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                          const __grid_constant__ AttnBwdParams p) {
@@ -497,7 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
   const bool carry_in = p.carry_in != 0;
-  const float* ld_smem = reinterpret_cast<const float*>(smem + OFF_LD);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KV_FULL), 1);
@@ -507,18 +521,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_DP_FULL), 1);
-    mbar_init(bar(B_P_FULL), kComputeWarps);
-    mbar_init(bar(B_DS_FULL), kComputeWarps);
+    mbar_init(bar(B_P_FULL), kCompute);
+    mbar_init(bar(B_DS_FULL), kCompute);
     mbar_init(bar(B_S_FREE), 1);
     mbar_init(bar(B_DP_FREE), 1);
-    mbar_init(bar(B_CARRY_READY), kComputeWarps);
+    mbar_init(bar(B_CARRY_READY), kCompute);
     mbar_init(bar(B_DKV_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN_G), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMma) {
     tmem_alloc(sb + OFF_TMEM_SLOT, kTmemCols);
     tmem_relinquish();
   }
@@ -527,10 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
 
-  if (warp == kProducerWarp) {
-    // Q and dO tiles (TMA) plus the tile's LSE/Delta records (bulk copy; the
-    // second is absent when the tile's upper 64 queries lie past L), all on
-    // one barrier per stage.
+  if (warp == kProducer) {
+    // Q and dO tiles (TMA), both on one barrier per stage.
     if (lane == 0) {
       int last[kStages];
 #pragma unroll
@@ -549,15 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (it / kStages) & 1;
         const int hl = kv * p.g_loc + it / nqt;
         const int qt = kb + it % nqt;
-        const int recs = 2 * qt + 1 < n_q64 ? 2 : 1;
         if (!mbar_wait(bar(B_QDO_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kTile + recs * kRec);
+        mbar_expect_tx(bar(B_QDO_FULL + s), 2 * kTile);
         tma_load_3d(sb + OFF_Q + s * kTile, &mq, bar(B_QDO_FULL + s), 0, qt * 128, p.q_z0 + hl);
         tma_load_3d(sb + OFF_Q + s * kTile + kHalf, &mq, bar(B_QDO_FULL + s), 64, qt * 128, p.q_z0 + hl);
         tma_load_3d(sb + OFF_DO + s * kTile, &mdo, bar(B_QDO_FULL + s), 0, qt * 128, p.do_z0 + hl);
         tma_load_3d(sb + OFF_DO + s * kTile + kHalf, &mdo, bar(B_QDO_FULL + s), 64, qt * 128, p.do_z0 + hl);
-        bulk_load(sb + OFF_LD + s * 2 * kRec, p.ld + (static_cast<int64_t>(hl) * n_q64 + 2 * qt) * 128, recs * kRec,
-                  bar(B_QDO_FULL + s));
         last[s] = it;
       }
       if (*abort_flag) {
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (last[s] >= 0) mbar_wait_drain(bar(B_QDO_FULL + s), (last[s] / kStages) & 1, p.status);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMma) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
       // Event-driven issue: S^T(i) once its Q/dO stage has landed and dV(i - 1)
@@ -608,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
-  } else if (warp == kGradWarp) {
+  } else if (warp == kGrad) {
     if (lane == 0) {
       // dV(i) += P^T(i) dO(i) once P^T is written (then the S^T columns are
       // free), dK(i) += dS^T(i) Q(i) once dS^T is written (then the dP^T
@@ -619,9 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bq = b_base + (it % kStages) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          // queries 16 kk .. 16 kk + 15: compute half kk / 4 wrote them at
-          // its own 64-column slice
-          const uint32_t a = tmem + tm_a + (kk >> 2) * 64 + (kk & 3) * 8;
+          // queries 16 kk .. 16 kk + 15: compute group kk / 2 wrote them at
+          // its own 32-column slice
+          const uint32_t a = tmem + tm_a + (kk >> 1) * 32 + (kk & 1) * 8;
           umma_bf16_ts(tmem + tm_d, a, sdesc_sw128(bq + kk * 2048, kHalf, 1024), id_g,
                        (carry_in || it > 0 || kk > 0) ? 1u : 0u);
         }
@@ -649,102 +658,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(B_DRAIN_G), 0, p.status);
     }
   } else {
-    // Compute warps: quadrant (warp & 3) of the key rows, half (warp >> 2) of
-    // the 128 query columns of each tile.
+    // Compute warps: quadrant (warp & 3) of the key rows, group (warp >> 2)
+    // of 32 query columns of each tile.
     const int quad = warp & 3;
-    const int half = warp >> 2;
+    const int grp = warp >> 2;
     const int r = quad * 32 + lane;  // key row = TMEM lane
     const int kpos = kb * 128 + r;
     const bool valid = kpos < p.L;
     const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
     const float sl2 = p.scale_log2;
-    // Warps 0-3 own dK, warps 4-7 own dV (carry load and epilogue).
-    float* my_carry = p.dkv_carry + (static_cast<int64_t>(kv * 2 + half) * p.L + kpos) * kHeadDim;
-    const int my_col = half == 0 ? TM_DK : TM_DV;
+    // Carry and epilogue: groups 0-1 own dK, 2-3 own dV, 64 columns each.
+    const int which = grp >> 1;
+    const int col0 = (grp & 1) * 64;
+    float* my_carry = p.dkv_carry + (static_cast<int64_t>(kv * 2 + which) * p.L + kpos) * kHeadDim + col0;
+    const uint32_t my_tm = trow + (which == 0 ? TM_DK : TM_DV) + col0;
     bool ok = true;
     if (carry_in) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 x = valid ? ld_global_nc_v4(my_carry + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
+          const uint4 x = valid ? ld_global_nc_v4(my_carry + c * 32 + q * 4) : make_uint4(0, 0, 0, 0);
           v[4 * q] = x.x;
           v[4 * q + 1] = x.y;
           v[4 * q + 2] = x.z;
           v[4 * q + 3] = x.w;
         }
-        tmem_st32(trow + my_col + c4 * 32, v);
+        tmem_st32(my_tm + c * 32, v);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_CARRY_READY));
     }
-    const uint32_t ts = trow + TM_ST + half * 64;
-    const uint32_t td = trow + TM_DPT + half * 64;
+    const uint32_t ts = trow + TM_ST + grp * 32;
+    const uint32_t td = trow + TM_DPT + grp * 32;
     for (int it = 0; it < n_it; ++it) {
-      const int qs = it % kStages;
+      const int hl = kv * p.g_loc + it / nqt;
       const int qt = kb + it % nqt;
-      const int q0 = qt * 128 + half * 64;  // query of this warp's first column
+      const int q0 = qt * 128 + grp * 32;  // query of this warp's first column
       // Without its record (all 64 queries past L) the slice is all zero.
-      const bool live = 2 * qt + half < n_q64;
-      const float* rec = ld_smem + qs * 256 + half * 128;
-      // ---- phase 1: P^T over the S^T columns
+      const bool live = 2 * qt + (grp >> 1) < n_q64;
+      // This warp's 32 queries in their record: -LSE*log2(e) at +0, Delta at +64.
+      const float* rec = p.ld + (static_cast<int64_t>(hl) * n_q64 + 2 * qt + (grp >> 1)) * 128 + (grp & 1) * 32;
+      if (live) {
+        prefetch_l1(rec);
+        prefetch_l1(rec + 64);
+      }
+      // ---- phase 1: P^T over the S^T columns, 16 at a time; the packed
+      // P^T of columns 16 h .. 16 h + 15 goes to columns 8 h .. 8 h + 7, which
+      // this warp has already read.
       if (!(ok = warp_wait(bar(B_S_FULL), it & 1, w))) break;
-      if (!(ok = warp_wait(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
       tc_fence_after();
-      float pf[64];
-      {
-        uint32_t s0[32], s1[32];
-        tmem_ld32(ts, s0);
-        tmem_ld32(ts + 32, s1);
-        tmem_ld_wait(s0);
-        tmem_ld_wait(s1);
-        uint32_t pk0[16], pk1[16];
+      float pf[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 l4[4];
+        load_rec16(rec + 16 * h, live, l4);
+        uint32_t sv[16];
+        tmem_ld16(ts + 16 * h, sv);
+        tmem_ld_wait(sv);
         if (!live) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pf[c] = 0.f;
+          for (int c = 0; c < 16; ++c) pf[16 * h + c] = 0.f;
         } else if (qt == kb) {  // the diagonal tile (warp-uniform)
-          p_slice<true>(s0, rec, sl2, q0, kpos, pf);
-          p_slice<true>(s1, rec + 32, sl2, q0 + 32, kpos, pf + 32);
+          p_slice<true>(sv, l4, sl2, q0 + 16 * h, kpos, pf + 16 * h);
         } else {
-          p_slice<false>(s0, rec, sl2, q0, kpos, pf);
-          p_slice<false>(s1, rec + 32, sl2, q0 + 32, kpos, pf + 32);
+          p_slice<false>(sv, l4, sl2, q0 + 16 * h, kpos, pf + 16 * h);
         }
+        uint32_t pk[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          pk0[c] = pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
-          pk1[c] = pack_bf16x2(pf[32 + 2 * c], pf[32 + 2 * c + 1]);
-        }
-        tmem_st16(ts, pk0);
-        tmem_st16(ts + 16, pk1);
-        tmem_st_wait();
+        for (int c = 0; c < 8; ++c) pk[c] = pack_bf16x2(pf[16 * h + 2 * c], pf[16 * h + 2 * c + 1]);
+        tmem_st8(ts + 8 * h, pk);
       }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL));
       // ---- phase 2: dS^T = P^T * (dP^T - Delta) over the dP^T columns
       if (!(ok = warp_wait(bar(B_DP_FULL), it & 1, w))) break;
       tc_fence_after();
-      {
-        uint32_t d0[32], d1[32];
-        tmem_ld32(td, d0);
-        tmem_ld32(td + 32, d1);
-        tmem_ld_wait(d0);
-        tmem_ld_wait(d1);
-        uint32_t dd0[16], dd1[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float4 d4[4];
+        load_rec16(rec + 64 + 16 * h, live, d4);
+        uint32_t dv[16];
+        tmem_ld16(td + 16 * h, dv);
+        tmem_ld_wait(dv);
+        uint32_t dd[8];
         if (!live) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dd0[c] = dd1[c] = 0u;
+          for (int c = 0; c < 8; ++c) dd[c] = 0u;
         } else {
-          dst_slice(d0, pf, rec + 64, dd0);
-          dst_slice(d1, pf + 32, rec + 96, dd1);
+          dst_slice(dv, pf + 16 * h, d4, dd);
         }
-        tmem_st16(td, dd0);
-        tmem_st16(td + 16, dd1);
-        tmem_st_wait();
+        tmem_st8(td + 8 * h, dd);
       }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS_FULL));
@@ -754,34 +765,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (p.carry_out) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(trow + my_col + c4 * 32, v);
+          tmem_ld32(my_tm + c * 32, v);
           tmem_ld_wait(v);
           if (valid) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              st_global_v4(my_carry + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              st_global_v4(my_carry + c * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
-      } else if (half == 0) {
+      } else if (which == 0) {
         // dK: scale, rotate back by -angle (layer path), bf16 (+ residual).
+        // This warp writes the RoPE pairs (i, i + 64), i in [32 (grp & 1), +32).
         __nv_bfloat16* outk = p.dk + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head;
         const float2* tab = p.rope ? p.rope + static_cast<int64_t>(kpos) * 64 : nullptr;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t a[32], b[32];
-          tmem_ld32(trow + TM_DK + hh * 32, a);
-          tmem_ld32(trow + TM_DK + 64 + hh * 32, b);
+          const int i0 = (grp & 1) * 32 + hh * 16;
+          uint32_t a[16], b[16];
+          tmem_ld16(trow + TM_DK + i0, a);
+          tmem_ld16(trow + TM_DK + 64 + i0, b);
           tmem_ld_wait(a);
           tmem_ld_wait(b);
-          float lo[32], hi[32];
+          float lo[16], hi[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const float x0 = __uint_as_float(a[i]) * p.scale;
             const float x1 = __uint_as_float(b[i]) * p.scale;
             if (tab && valid) {
-              const float2 cs = tab[hh * 32 + i];
+              const float2 cs = tab[i0 + i];
               lo[i] = x0 * cs.x + x1 * cs.y;
               hi[i] = x1 * cs.x - x0 * cs.y;
             } else {
@@ -791,25 +804,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (valid) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              store8_bf16_split(outk + hh * 32 + q * 8, lo + 8 * q, p.lo_off);
-              store8_bf16_split(outk + 64 + hh * 32 + q * 8, hi + 8 * q, p.lo_off);
+            for (int q = 0; q < 2; ++q) {
+              store8_bf16_split(outk + i0 + q * 8, lo + 8 * q, p.lo_off);
+              store8_bf16_split(outk + 64 + i0 + q * 8, hi + 8 * q, p.lo_off);
             }
           }
         }
       } else {
-        __nv_bfloat16* outv = p.dv + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head;
+        __nv_bfloat16* outv =
+            p.dv + static_cast<int64_t>(kpos) * p.dkv_row + static_cast<int64_t>(kv) * p.dkv_head + col0;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(trow + TM_DV + c4 * 32, v);
+          tmem_ld32(my_tm + c * 32, v);
           tmem_ld_wait(v);
           if (valid) {
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) store8_bf16_split(outv + c4 * 32 + q * 8, f + 8 * q, p.lo_off);
+            for (int q = 0; q < 4; ++q) store8_bf16_split(outv + c * 32 + q * 8, f + 8 * q, p.lo_off);
           }
         }
       }
@@ -818,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -842,7 +856,7 @@ cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q, const CUtensorMap& k, con
       cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(n_kblocks, p.nkv);
-  attn_bwd_dkdv_kernel<<<grid, kThreads, dkv::kSmemBytes, s>>>(q, k, v, dO, p);
+  attn_bwd_dkdv_kernel<<<grid, dkv::kThreadsKv, dkv::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }
 

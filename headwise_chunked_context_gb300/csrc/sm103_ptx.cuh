@@ -21,11 +21,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
+// SM cycle counter, used to bound waits.  It is cheap to read, unlike
+// %globaltimer, whose read can hold a polling warp for about a thousand
+// cycles and so delay its noticing a completed barrier phase.  Limits are
+// given in nanoseconds and compared against cycles at an assumed clock of at
+// most 3 GHz, so a wait lasts at least its limit in wall time at any real
+// SM clock.
+__device__ __forceinline__ uint64_t sm_cycles() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
   return t;
 }
+constexpr uint64_t kCyclesPerNs = 3;
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -92,11 +99,11 @@ struct WaitCtl {
 // flag and records a timeout) or another thread of the CTA aborted first.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = sm_cycles();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort_flag) return false;
-    if (global_timer_ns() - t0 > w.limit_ns) {
+    if (sm_cycles() - t0 > w.limit_ns * kCyclesPerNs) {
       *w.abort_flag = 1;
       atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
       return false;
@@ -113,10 +120,10 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, const W
     if (mbar_test(bar, parity)) return true;
     if ((i & 31) != 0) continue;  // the abort flag and the clock every 32 polls
     if (*w.abort_flag) return false;
-    const uint64_t now = global_timer_ns();
+    const uint64_t now = sm_cycles();
     if (i == 32) {
       t0 = now;
-    } else if (now - t0 > w.limit_ns) {
+    } else if (now - t0 > w.limit_ns * kCyclesPerNs) {
       *w.abort_flag = 1;
       atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
       return false;
@@ -128,9 +135,9 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, const W
 // limit.  Used only on events that complete without help from other threads
 // (TMA bytes landing, issued MMAs retiring).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* status) {
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = sm_cycles();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > 1000000000ull) {
+    if (sm_cycles() - t0 > 1000000000ull * kCyclesPerNs) {
       atomicOr(status, UPIPE_STATUS_DRAIN_TIMEOUT);
       return false;
     }
@@ -154,8 +161,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 // non-blocking probes and issues whatever is ready: `alive` turns false
 // (raising the abort flag and the timeout status) once `limit_ns` passes
 // without progress, or as soon as another thread of the CTA aborted.  The
-// clock (a slow special-register read) is sampled only every 32 idle polls,
-// so that a poll that finds work ready reacts within a few cycles.
+// abort flag and the clock are read only every 32 idle polls, so that a poll
+// that finds work ready reacts within a few cycles.
 struct Watchdog {
   uint64_t t0;
   uint32_t idle;
@@ -163,10 +170,10 @@ struct Watchdog {
   __device__ __forceinline__ bool alive(const WaitCtl& w) {
     if ((++idle & 31) != 0) return true;  // the abort flag and the clock every 32 idle polls
     if (*w.abort_flag) return false;
-    const uint64_t now = global_timer_ns();
+    const uint64_t now = sm_cycles();
     if (idle == 32) {
       t0 = now;
-    } else if (now - t0 > w.limit_ns) {
+    } else if (now - t0 > w.limit_ns * kCyclesPerNs) {
       *w.abort_flag = 1;
       atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
       return false;
@@ -176,6 +183,11 @@ struct Watchdog {
 };
 
 // --------------------------------------------------------------------- TMA
+
+// Pulls the 128-byte line holding `p` into L1.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
+}
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -314,6 +326,18 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : UPIPE_R8(0), UPIPE_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : UPIPE_P8(0), UPIPE_P8(8)::"memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -329,6 +353,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

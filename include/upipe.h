@@ -53,8 +53,11 @@
  * Every entry point returns 0 on success or a negative UPIPE_ERR_* code.
  * Argument errors are detected on the host before anything is enqueued.
  * Device-side waits are bounded (default 2 s, environment variable
- * UPIPE_SPIN_LIMIT_NS overrides); a wait that runs out makes its kernel
- * unwind and sets a device status word, read by upipe_last_device_status().
+ * UPIPE_SPIN_LIMIT_NS overrides; kernels count the limit in SM clock cycles
+ * at 3 cycles per nanosecond, so at clocks below 3 GHz a wait lasts somewhat
+ * longer than the limit, never shorter); a wait that runs out makes its
+ * kernel unwind and sets a device status word, read by
+ * upipe_last_device_status().
  */
 #ifndef UPIPE_H_
 #define UPIPE_H_
