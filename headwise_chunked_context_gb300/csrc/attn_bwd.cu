@@ -20,28 +20,25 @@
 //    are carried in fp32 between chunks and reloaded into TMEM, which keeps
 //    the same order as a single pass over the whole group.
 //
-// Both kernels: warp 8 loads tiles with TMA (the dkdv producer also copies
-// the query tile's LSE/Delta records), warp 9 issues the products of
-// shared-memory operands (S, dP), warp 10 the products that read the
-// softmax tiles from TMEM (dQ, dV, dK), and warps 0-7
-// turn scores into P / dS: two warps share each TMEM lane quadrant and split
-// the columns, so every SM sub-partition has two of them to hide latency.
-// The tensor core reads shared-memory operands at about 128 B/clk per SM, so
-// the softmax tiles (P^T, dS^T, dS) stay in TMEM and feed the products that
-// consume them as TMEM A operands.
+// Both kernels have one producer warp loading tiles with TMA, one issuing
+// warp per product kind (a single thread issues a tcgen05.mma only about
+// every 100 cycles), and compute warps that turn scores into P / dS.  Warp w
+// of the compute warps reads TMEM lane quadrant w % 4, so the warps sharing a
+// quadrant split its columns.  Shared-memory operand reads run at roughly
+// 80-100 B/clk per SM, so the softmax tiles (P^T, dS^T, dS) stay in TMEM and
+// feed the products that consume them as TMEM A operands.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
 namespace {
 
-// 8 compute warps, 1 producer warp and 2 MMA-issuing warps: one thread
-// issues a tcgen05.mma about every 100 cycles at best, so two threads, each
-// owning its own accumulators, keep the tensor core busy.
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;    // products from shared-memory operands (S, dP)
-constexpr int kGradWarp = 10;  // products that consume the softmax tiles from TMEM
+// Warp roles of the dq kernel (the dkdv kernel has its own, below).  One
+// thread issues a tcgen05.mma about every 100 cycles at best, so each product
+// kind has its own issuing warp, owning its own accumulators.
 constexpr int kComputeWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;    // issues S; allocates TMEM
+constexpr int kGradWarp = 10;  // issues dQ, which consumes dS from TMEM
 constexpr uint32_t kTmemCols = 512;
 
 // dS row slice of the dq kernel: 32 keys of one query row, paired fp32
@@ -130,24 +127,27 @@ __device__ __forceinline__ void load_rec16(const float* p, bool live, float4 (&v
 // that the compute warps release as soon as they have read it; the compute
 // warps write dS (packed bf16) over the S columns they have read, and
 // dQ += dS K takes dS straight from TMEM.  K and V stream through separate
-// two-stage TMA rings (V is released after dP, K after dQ).
+// TMA rings: V is released after dP (two stages suffice), K only after dQ,
+// about a block later, so its ring has three.  S, dP and dQ each have their
+// own issuing warp.
 
 namespace dq {
 constexpr int kTile = 128 * 128 * 2;   // [128][128] bf16 as two 64-column halves
 constexpr int kHalf = kTile / 2;
-constexpr int kStages = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTile;
-constexpr int OFF_K = OFF_DO + kTile;             // kStages
-constexpr int OFF_V = OFF_K + kStages * kTile;    // kStages
-constexpr int OFF_BAR = OFF_V + kStages * kTile;
+constexpr int OFF_K = OFF_DO + kTile;              // kKStages
+constexpr int OFF_V = OFF_K + kKStages * kTile;    // kVStages
+constexpr int OFF_BAR = OFF_V + kVStages * kTile;
 enum {
   B_QDO_FULL,
   B_K_FULL,
-  B_K_EMPTY = B_K_FULL + kStages,
-  B_V_FULL = B_K_EMPTY + kStages,
-  B_V_EMPTY = B_V_FULL + kStages,
-  B_S_FULL = B_V_EMPTY + kStages,
+  B_K_EMPTY = B_K_FULL + kKStages,
+  B_V_FULL = B_K_EMPTY + kKStages,
+  B_V_EMPTY = B_V_FULL + kVStages,
+  B_S_FULL = B_V_EMPTY + kVStages,
   B_S_FREE = B_S_FULL + 2,   // dQ of that buffer done: its S/dS columns free
   B_DS_FULL = B_S_FREE + 2,
   B_DP_FULL = B_DS_FULL + 2,
@@ -155,15 +155,20 @@ enum {
   B_DQ_DONE,
   B_DRAIN,
   B_DRAIN_G,
+  B_DRAIN_P,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
 constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "dq kernel shared memory");
 constexpr int TM_S = 0, TM_DP = 256, TM_DQ = 384;  // S: two 128-column buffers
+// Warps 0-7 compute, 8 producer, 9 issues S, 10 issues dQ, 11 issues dP.
+constexpr int kDpWarp = 11;
+constexpr int kThreadsDq = 384;
 }  // namespace dq
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dq::kThreadsDq, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                        const __grid_constant__ AttnBwdParams p) {
@@ -184,9 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QDO_FULL), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(B_K_FULL + s), 1);
       mbar_init(bar(B_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(B_V_FULL + s), 1);
       mbar_init(bar(B_V_EMPTY + s), 1);
     }
@@ -200,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DQ_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN_G), 1);
+    mbar_init(bar(B_DRAIN_P), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -223,31 +231,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sb + OFF_Q + kHalf, &mq, bar(B_QDO_FULL), 64, qb * 128, p.q_z0 + h);
       tma_load_3d(sb + OFF_DO, &mdo, bar(B_QDO_FULL), 0, qb * 128, p.do_z0 + h);
       tma_load_3d(sb + OFF_DO + kHalf, &mdo, bar(B_QDO_FULL), 64, qb * 128, p.do_z0 + h);
-      int last_k[kStages], last_v[kStages];
+      int last_k[kKStages], last_v[kVStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_k[s] = last_v[s] = -1;
-      // V(j) frees earlier than K(j), so V runs one block ahead of K.
+      for (int s = 0; s < kKStages; ++s) last_k[s] = -1;
+#pragma unroll
+      for (int s = 0; s < kVStages; ++s) last_v[s] = -1;
+      // Whichever ring has a free stage gets its next block, K first (S(j)
+      // needs K(j) before dP(j) needs V(j)).
       int nk = 0, nv = 0;
       Watchdog wd;
       wd.reset();
       bool ok = true;
       while (ok && (nk < n_kv || nv < n_kv)) {
         bool did = false;
-        if (nv < n_kv && nv <= nk + 1 &&
-            mbar_test(bar(B_V_EMPTY + nv % kStages), ((nv / kStages) & 1) ^ 1)) {
-          const int s = nv % kStages;
-          mbar_expect_tx(bar(B_V_FULL + s), kTile);
-          tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, nv * 128, vz);
-          tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, nv * 128, vz);
-          last_v[s] = nv++;
-          did = true;
-        }
-        if (nk < n_kv && mbar_test(bar(B_K_EMPTY + nk % kStages), ((nk / kStages) & 1) ^ 1)) {
-          const int s = nk % kStages;
+        if (nk < n_kv && mbar_test(bar(B_K_EMPTY + nk % kKStages), ((nk / kKStages) & 1) ^ 1)) {
+          const int s = nk % kKStages;
           mbar_expect_tx(bar(B_K_FULL + s), kTile);
           tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, nk * 128, kz);
           tma_load_3d(sb + OFF_K + s * kTile + kHalf, &mk, bar(B_K_FULL + s), 64, nk * 128, kz);
           last_k[s] = nk++;
+          did = true;
+        }
+        if (nv < n_kv && mbar_test(bar(B_V_EMPTY + nv % kVStages), ((nv / kVStages) & 1) ^ 1)) {
+          const int s = nv % kVStages;
+          mbar_expect_tx(bar(B_V_FULL + s), kTile);
+          tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, nv * 128, vz);
+          tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, nv * 128, vz);
+          last_v[s] = nv++;
           did = true;
         }
         if (did) wd.reset();
@@ -255,28 +265,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         mbar_wait_drain(bar(B_QDO_FULL), 0, p.status);
-        for (int s = 0; s < kStages; ++s) {
-          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] / kStages) & 1, p.status);
-          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] / kStages) & 1, p.status);
-        }
+        for (int s = 0; s < kKStages; ++s)
+          if (last_k[s] >= 0) mbar_wait_drain(bar(B_K_FULL + s), (last_k[s] / kKStages) & 1, p.status);
+        for (int s = 0; s < kVStages; ++s)
+          if (last_v[s] >= 0) mbar_wait_drain(bar(B_V_FULL + s), (last_v[s] / kVStages) & 1, p.status);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
-      // Event-driven issue of S(ns) once K(ns) has landed and dQ(ns - 2) has
-      // released the buffer, and dP(nd) once V(nd) has landed and dP(nd - 1)
-      // has been read.
-      auto s_ready = [&](int j) {
-        return mbar_test(bar(B_K_FULL + j % kStages), (j / kStages) & 1) &&
-               mbar_test(bar(B_S_FREE + (j & 1)), ((j >> 1) & 1) ^ 1);
-      };
-      auto dp_ready = [&](int j) {
-        return mbar_test(bar(B_V_FULL + j % kStages), (j / kStages) & 1) &&
-               mbar_test(bar(B_DP_EMPTY), (j & 1) ^ 1);
-      };
-      auto issue_s = [&](int j) {
-        const uint32_t ka = sb + OFF_K + (j % kStages) * kTile;
+      // S(j) = Q K(j)^T into buffer j & 1 once K(j) has landed and dQ(j - 2)
+      // has released the buffer.
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);
+      bool ok = mbar_spin(bar(B_QDO_FULL), 0, w);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % kKStages;
+        if (!(ok = mbar_spin(bar(B_K_FULL + s), (j / kKStages) & 1, w))) break;
+        if (!(ok = mbar_spin(bar(B_S_FREE + (j & 1)), ((j >> 1) & 1) ^ 1, w))) break;
+        tc_fence_after();
+        const uint32_t ka = sb + OFF_K + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -284,9 +290,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sdesc_sw128(ka + off, 16, 1024), id_kk, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(B_S_FULL + (j & 1)));
-      };
-      auto issue_dp = [&](int j) {
-        const int s = j % kStages;
+      }
+      umma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, p.status);
+    }
+  } else if (warp == kDpWarp) {
+    if (lane == 0) {
+      // dP(j) = dO V(j)^T once V(j) has landed and dP(j - 1) has been read.
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);
+      bool ok = mbar_spin(bar(B_QDO_FULL), 0, w);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % kVStages;
+        if (!(ok = mbar_spin(bar(B_V_FULL + s), (j / kVStages) & 1, w))) break;
+        if (!(ok = mbar_spin(bar(B_DP_EMPTY), (j & 1) ^ 1, w))) break;
+        tc_fence_after();
         const uint32_t va = sb + OFF_V + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -296,38 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(bar(B_DP_FULL));
         umma_commit(bar(B_V_EMPTY + s));
-      };
-      bool ok = mbar_wait(bar(B_QDO_FULL), 0, w);
-      int ns = 0, nd = 0;
-      Watchdog wd;
-      wd.reset();
-      while (ok && nd < n_kv) {
-        bool did = false;
-        if (ns < n_kv && ns <= nd + 1 && s_ready(ns)) {
-          tc_fence_after();
-          issue_s(ns++);
-          did = true;
-        }
-        if (nd < ns && dp_ready(nd)) {
-          tc_fence_after();
-          issue_dp(nd++);
-          did = true;
-        }
-        if (did) wd.reset();
-        else ok = wd.alive(w);
       }
-      umma_commit(bar(B_DRAIN));
-      mbar_wait_drain(bar(B_DRAIN), 0, p.status);
+      umma_commit(bar(B_DRAIN_P));
+      mbar_wait_drain(bar(B_DRAIN_P), 0, p.status);
     }
   } else if (warp == kGradWarp) {
     if (lane == 0) {
       // dQ(j) += dS(j) K(j) once dS(j) is written; then S buffer j & 1 and
-      // K stage j % kStages are free (S(j) had completed before dS(j) existed).
+      // K stage j % kKStages are free (S(j) had completed before dS(j) existed).
       constexpr uint32_t id_q = idesc_bf16(128, 128, 0, 1);  // dS from TMEM, K MN-major
       bool ok = true;
       for (int j = 0; ok && j < n_kv; ++j) {
         const int b = j & 1;
-        const int s = j % kStages;
+        const int s = j % kKStages;
         if (!(ok = mbar_spin(bar(B_DS_FULL + b), (j >> 1) & 1, w))) break;
         tc_fence_after();
         const uint32_t ka = sb + OFF_K + s * kTile;
@@ -846,7 +844,7 @@ cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(n_qblocks, p.nheads);
-  attn_bwd_dq_kernel<<<grid, kThreads, dq::kSmemBytes, s>>>(q, k, v, dO, p);
+  attn_bwd_dq_kernel<<<grid, dq::kThreadsDq, dq::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }
 
