@@ -14,15 +14,16 @@
 //    first so the causal triangle balances across SMs;
 //  * warp 4 streams Q once and K/V blocks of 128 keys through 3-stage TMA
 //    rings (128-byte swizzle); the softmax warps copy Q into TMEM once;
-//  * warp 5 issues S(j) = Q K^T (Q from TMEM) into one of two TMEM score
-//    buffers; warp 6 issues O += P V (P from TMEM).  A thread issues a
-//    tcgen05.mma only about every 100 cycles, hence two issuers;
+//  * warp 5 issues S(j) = Q K^T (Q from TMEM) into the TMEM score buffer;
+//    warp 6 issues O += P V (P from TMEM).  A thread issues a tcgen05.mma
+//    only about every 100 cycles, hence two issuers;
 //  * warps 0-3 own one query row per thread (the TMEM lane), so row max and
-//    row sum are thread-local; they write P as packed bf16 into a TMEM
-//    buffer of its own, so a score buffer is free again as soon as it has
-//    been read, and S(j + 2) overlaps the softmax of block j.  O is rescaled
-//    in TMEM only when a row maximum grows by more than 2^8, which bounds
-//    every exponent and keeps the result exact up to rounding.
+//    row sum are thread-local.  They write P as packed bf16 into one of two
+//    TMEM buffers of its own: the score buffer is free again as soon as it
+//    has been read (S(j + 1) overlaps the rest of the softmax of block j),
+//    and P(j) need not wait for P V of block j - 1.  O is rescaled in TMEM
+//    only when a row maximum grows by more than 2^8, which bounds every
+//    exponent and keeps the result exact up to rounding.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -44,10 +45,10 @@ enum {
   B_V_FULL = B_K_EMPTY + kStages,
   B_V_EMPTY = B_V_FULL + kStages,
   B_S_FULL = B_V_EMPTY + kStages,
-  B_S_READ = B_S_FULL + 2,   // the softmax warps have read that score buffer
-  B_P_FULL = B_S_READ + 2,   // P written (one buffer)
-  B_P_EMPTY,                 // P V done: P buffer free, O up to date
-  B_DRAIN,
+  B_S_READ,                  // the softmax warps have read the score buffer
+  B_P_FULL,                  // P written, per P buffer
+  B_P_EMPTY = B_P_FULL + 2,  // P V done: that P buffer free, O up to date
+  B_DRAIN = B_P_EMPTY + 2,
   B_DRAIN_PV,
   B_COUNT
 };
@@ -58,9 +59,9 @@ constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;  // + alignment slack
 constexpr int kThreads = 224;  // softmax warps 0-3, producer 4, S issuer 5, PV issuer 6
 constexpr uint32_t kTmemCols = 512;
 constexpr int TM_Q = 0;    // Q, packed bf16: columns [0, 64)
-constexpr int TM_S = 64;   // two score buffers of 128 columns: [64, 320)
-constexpr int TM_O = 320;  // O accumulator: [320, 448)
-constexpr int TM_P = 448;  // P, packed bf16: [448, 512)
+constexpr int TM_S = 64;   // scores: [64, 192)
+constexpr int TM_O = 192;  // O accumulator: [192, 320)
+constexpr int TM_P = 320;  // two P buffers, packed bf16: [320, 384), [384, 448)
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -88,12 +89,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_V_FULL + s), 1);
       mbar_init(bar(B_V_EMPTY + s), 1);
     }
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_S_READ), 4);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_S_FULL + b), 1);
-      mbar_init(bar(B_S_READ + b), 4);
+      mbar_init(bar(B_P_FULL + b), 4);
+      mbar_init(bar(B_P_EMPTY + b), 1);
     }
-    mbar_init(bar(B_P_FULL), 4);
-    mbar_init(bar(B_P_EMPTY), 1);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN_PV), 1);
     *abort_flag = 0;
@@ -146,22 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q (TMEM) x K (smem, K-major)
-      // S(j) once K(j) has landed and the softmax warps have read S(j - 2)
-      // out of the same buffer.
+      // S(j) once K(j) has landed and the softmax warps have read S(j - 1).
       bool ok = mbar_spin(bar(B_Q_TMEM), 0, w);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int b = j & 1;
         const int s = j % kStages;
         if (!(ok = mbar_spin(bar(B_K_FULL + s), (j / kStages) & 1, w))) break;
-        if (!(ok = mbar_spin(bar(B_S_READ + b), ((j >> 1) & 1) ^ 1, w))) break;
+        if (!(ok = mbar_spin(bar(B_S_READ), (j & 1) ^ 1, w))) break;
         tc_fence_after();
         const uint32_t ka = sb + OFF_K + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16_ts(tmem + TM_S + b * 128, tmem + TM_Q + kk * 8,
+          umma_bf16_ts(tmem + TM_S, tmem + TM_Q + kk * 8,
                        sdesc_sw128(ka + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_S_FULL + b));
+        umma_commit(bar(B_S_FULL));
         umma_commit(bar(B_K_EMPTY + s));
       }
       umma_commit(bar(B_DRAIN));
@@ -173,17 +172,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (TMEM) x V (smem, MN-major)
       bool ok = true;
       for (int j = 0; ok && j < n_kv; ++j) {
+        const int b = j & 1;
         const int s = j % kStages;
-        if (!(ok = mbar_spin(bar(B_P_FULL), j & 1, w))) break;
+        if (!(ok = mbar_spin(bar(B_P_FULL + b), (j >> 1) & 1, w))) break;
         if (!(ok = mbar_spin(bar(B_V_FULL + s), (j / kStages) & 1, w))) break;
         tc_fence_after();
         const uint32_t va = sb + OFF_V + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_bf16_ts(tmem + TM_O, tmem + TM_P + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_o,
+          umma_bf16_ts(tmem + TM_O, tmem + TM_P + b * 64 + kk * 8, sdesc_sw128(va + kk * 2048, kHalf, 1024), id_o,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_P_EMPTY));
+        umma_commit(bar(B_P_EMPTY + b));
         umma_commit(bar(B_V_EMPTY + s));
       }
       umma_commit(bar(B_DRAIN_PV));
@@ -219,11 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_Q_TMEM));
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!(ok = warp_wait(bar(B_S_FULL + b), ph, w))) break;
+      const int b = j & 1;  // P buffer
+      if (!(ok = warp_wait(bar(B_S_FULL), j & 1, w))) break;
       tc_fence_after();
-      const uint32_t tsb = trow + TM_S + b * 128;
+      const uint32_t tsb = trow + TM_S;
       uint32_t v0[32], v1[32], v2[32], v3[32];
       tmem_ld32(tsb + 0, v0);
       tmem_ld32(tsb + 32, v1);
@@ -235,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait(v3);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_READ + b));  // S(j + 2) may overwrite this buffer
+      if (lane == 0) mbar_arrive(bar(B_S_READ));  // S(j + 1) may overwrite the scores
 
       float x[128];
 #pragma unroll
@@ -264,13 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
       const float m_new = fmaxf(m_use, mx * sl2);
       const bool need = m_new > m_use + 8.0f;
-      // O and the P buffer hold PV(j - 1)'s operands and result until it
-      // completes: rescaling O or writing P(j) waits for it.
-      bool pv_done = j == 0;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds PV(0..j-1): rescale the rows that moved.
-        if (!(ok = warp_wait(bar(B_P_EMPTY), (j - 1) & 1, w))) break;
-        pv_done = true;
+        // O holds PV(0..j-1) once PV(j - 1) completes: rescale the rows
+        // that moved.
+        if (!(ok = warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, w))) break;
         tc_fence_after();
         const float f = need ? ex2_approx(m_use - m_new) : 1.f;
 #pragma unroll
@@ -310,18 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         rs += a + b;
       }
       l += rs;
-      if (!pv_done) {
-        if (!(ok = warp_wait(bar(B_P_EMPTY), (j - 1) & 1, w))) break;
+      // P buffer b held P(j - 2) until PV(j - 2) completed.
+      if (j >= 2) {
+        if (!(ok = warp_wait(bar(B_P_EMPTY + b), ((j >> 1) & 1) ^ 1, w))) break;
         tc_fence_after();
       }
-      tmem_st32(trow + TM_P + 0, pk0);
-      tmem_st32(trow + TM_P + 32, pk1);
+      tmem_st32(trow + TM_P + b * 64 + 0, pk0);
+      tmem_st32(trow + TM_P + b * 64 + 32, pk1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
     }
-    if (ok) ok = warp_wait(bar(B_P_EMPTY), (n_kv - 1) & 1, w);
+    // PV products complete in issue order: the last one completing means O is final.
+    if (ok) ok = warp_wait(bar(B_P_EMPTY + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, w);
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;

@@ -145,16 +145,31 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
-// Warp-wide wait: lane 0 polls (bounded), the outcome is broadcast, then
-// every lane observes the completed phase once itself (its own acquire), so
-// that only one lane per warp spins on the barrier word.  Must be called by
-// all 32 lanes; the result is warp-uniform.
+// Warp-wide wait: every lane probes the barrier each round and the warp moves
+// on once all lanes have seen the phase complete (each lane's own probe is
+// its acquire).  Free of divergence on purpose: a lane-0 poll loop followed
+// by a broadcast costs about 200 cycles even on a phase that completed long
+// ago, against about 15 for one warp-wide probe.  The abort flag and the
+// clock are checked every 32 rounds, by warp vote.  Must be called by all 32
+// lanes; the result is warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_spin(bar, parity, w) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) mbar_try_wait(bar, parity);
-  return ok != 0;
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    if ((i & 31) != 0) continue;
+    if (__any_sync(0xffffffffu, *w.abort_flag != 0)) return false;
+    const uint64_t now = sm_cycles();
+    if (i == 32) {
+      t0 = now;
+    } else if (__any_sync(0xffffffffu, now - t0 > w.limit_ns * kCyclesPerNs)) {
+      if ((threadIdx.x & 31) == 0) {
+        *w.abort_flag = 1;
+        atomicOr(w.status, UPIPE_STATUS_TIMEOUT);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
 }
 
 // No-progress watchdog for a thread that polls several barriers with
