@@ -65,58 +65,43 @@ __device__ __forceinline__ void ds_slice(const uint32_t (&sv)[32], const uint32_
   }
 }
 
-// P^T row slice of the dkdv kernel: 16 queries of one key row, kept in fp32
-// for the dS^T phase.  l4 holds the queries' -LSE * log2(e); kMask zeroes
+// P^T row slice of the dkdv kernel: 16 queries (columns c0 .. c0 + 15 of
+// this warp's 32) of one key row, kept in fp32 for the dS^T phase.  Lane c of
+// the warp holds -LSE * log2(e) of the warp's query c in `nl`; kMask zeroes
 // queries before the key (the diagonal tile only).
 template <bool kMask>
-__device__ __forceinline__ void p_slice(const uint32_t (&sv)[16], const float4 (&l4)[4], float sl2, int q0, int kpos,
+__device__ __forceinline__ void p_slice(const uint32_t (&sv)[16], float nl, int c0, float sl2, int q0, int kpos,
                                         float* pf) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    const float4 lv = l4[c4];
-    float t0, t1, t2, t3;
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])), sl2x2,
-                     f2_pack(lv.x, lv.y)),
-              t0, t1);
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])), sl2x2,
-                     f2_pack(lv.z, lv.w)),
-              t2, t3);
-    float p[4] = {ex2_approx(t0), ex2_approx(t1), ex2_approx(t2), ex2_approx(t3)};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (kMask && q0 + 4 * c4 + e < kpos) p[e] = 0.f;
-      pf[4 * c4 + e] = p[e];
+  for (int c = 0; c < 16; c += 2) {
+    const float l0 = __shfl_sync(0xffffffffu, nl, c0 + c);
+    const float l1 = __shfl_sync(0xffffffffu, nl, c0 + c + 1);
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, f2_pack(l0, l1)), t0, t1);
+    float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+    if (kMask) {
+      if (q0 + c0 + c < kpos) p0 = 0.f;
+      if (q0 + c0 + c + 1 < kpos) p1 = 0.f;
     }
+    pf[c] = p0;
+    pf[c + 1] = p1;
   }
 }
 
-// dS^T row slice of the dkdv kernel: dS = P * (dP - Delta) for 16 queries,
-// packed bf16.  d4 holds the queries' Delta.
-__device__ __forceinline__ void dst_slice(const uint32_t (&dv)[16], const float* pf, const float4 (&d4)[4],
+// dS^T row slice of the dkdv kernel: dS = P * (dP - Delta) for 16 queries
+// (columns c0 .. c0 + 15), packed bf16.  Lane c holds Delta of query c in `dl`.
+__device__ __forceinline__ void dst_slice(const uint32_t (&dv)[16], const float* pf, float dl, int c0,
                                           uint32_t (&dd)[8]) {
 #pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    const float4 dl = d4[c4];
-    float s0, s1, s2, s3;
-    f2_unpack(f2_mul(f2_pack(pf[4 * c4], pf[4 * c4 + 1]),
-                     f2_sub(f2_pack(__uint_as_float(dv[4 * c4]), __uint_as_float(dv[4 * c4 + 1])), f2_pack(dl.x, dl.y))),
+  for (int c = 0; c < 16; c += 2) {
+    const float d0 = __shfl_sync(0xffffffffu, dl, c0 + c);
+    const float d1 = __shfl_sync(0xffffffffu, dl, c0 + c + 1);
+    float s0, s1;
+    f2_unpack(f2_mul(f2_pack(pf[c], pf[c + 1]),
+                     f2_sub(f2_pack(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), f2_pack(d0, d1))),
               s0, s1);
-    f2_unpack(f2_mul(f2_pack(pf[4 * c4 + 2], pf[4 * c4 + 3]),
-                     f2_sub(f2_pack(__uint_as_float(dv[4 * c4 + 2]), __uint_as_float(dv[4 * c4 + 3])),
-                            f2_pack(dl.z, dl.w))),
-              s2, s3);
-    dd[2 * c4] = pack_bf16x2(s0, s1);
-    dd[2 * c4 + 1] = pack_bf16x2(s2, s3);
-  }
-}
-
-// Four float4 of a record (16 consecutive floats) from global memory.
-__device__ __forceinline__ void load_rec16(const float* p, bool live, float4 (&v)[4]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 x = live ? ld_global_nc_v4(p + 4 * c) : make_uint4(0, 0, 0, 0);
-    v[c] = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w));
+    dd[c >> 1] = pack_bf16x2(s0, s1);
   }
 }
 
@@ -464,16 +449,17 @@ enum {
   B_KV_FULL,
   B_QDO_FULL,
   B_QDO_EMPTY = B_QDO_FULL + kStages,
-  B_S_FULL = B_QDO_EMPTY + kStages,
-  B_DP_FULL,
-  B_P_FULL,    // P^T written (compute warps)
+  B_S_FULL = B_QDO_EMPTY + kStages,  // per 64-query half of S^T
+  B_P_FULL = B_S_FULL + 2,           // P^T of that half written (its 8 compute warps)
+  B_S_FREE = B_P_FULL + 2,           // dV of that half done: its S^T / P^T columns free
+  B_DP_FULL = B_S_FREE + 2,
   B_DS_FULL,   // dS^T written (compute warps)
-  B_S_FREE,    // dV done: S^T / P^T columns free
   B_DP_FREE,   // dK done: dP^T / dS^T columns free
   B_CARRY_READY,
   B_DKV_DONE,
   B_DRAIN,
   B_DRAIN_G,
+  B_DRAIN_P,
   B_COUNT
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
@@ -482,12 +468,14 @@ constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
 constexpr int TM_ST = 0, TM_DPT = 128, TM_DV = 256, TM_DK = 384;
 // 16 compute warps: four per TMEM lane quadrant, each owning 32 of the 128
 // query columns, so each SM sub-partition has four to hide TMEM and exp2
-// latency; then the producer and the two MMA-issuing warps.
+// latency; then the producer and three MMA-issuing warps (S^T; dV and dK;
+// dP^T).
 constexpr int kCompute = 16;
 constexpr int kProducer = 16;
 constexpr int kMma = 17;
 constexpr int kGrad = 18;
-constexpr int kThreadsKv = 608;
+constexpr int kDpMma = 19;
+constexpr int kThreadsKv = 640;
 }  // namespace dkv
 
 __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
@@ -517,16 +505,19 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       mbar_init(bar(B_QDO_FULL + s), 1);
       mbar_init(bar(B_QDO_EMPTY + s), 1);
     }
-    mbar_init(bar(B_S_FULL), 1);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(bar(B_S_FULL + hf), 1);
+      mbar_init(bar(B_P_FULL + hf), kCompute / 2);
+      mbar_init(bar(B_S_FREE + hf), 1);
+    }
     mbar_init(bar(B_DP_FULL), 1);
-    mbar_init(bar(B_P_FULL), kCompute);
     mbar_init(bar(B_DS_FULL), kCompute);
-    mbar_init(bar(B_S_FREE), 1);
     mbar_init(bar(B_DP_FREE), 1);
     mbar_init(bar(B_CARRY_READY), kCompute);
     mbar_init(bar(B_DKV_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN_G), 1);
+    mbar_init(bar(B_DRAIN_P), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -575,57 +566,64 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
     }
   } else if (warp == kMma) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
-      // Event-driven issue: S^T(i) once its Q/dO stage has landed and dV(i - 1)
-      // is done; dP^T(i) once dK(i - 1) is done.
-      auto qdo_full = [&](int it) { return mbar_test(bar(B_QDO_FULL + it % kStages), (it / kStages) & 1); };
-      auto s_ready = [&](int it) { return qdo_full(it) && mbar_test(bar(B_S_FREE), (it & 1) ^ 1); };
-      auto dp_ready = [&](int it) { return qdo_full(it) && mbar_test(bar(B_DP_FREE), (it & 1) ^ 1); };
-      auto issue_kq = [&](int it, uint32_t a_base, uint32_t b_base, int tm, int done) {
-        const uint32_t bq = b_base + (it % kStages) * kTile;
+      // S^T(i) in two 64-query halves (N=64): half h once the Q/dO stage has
+      // landed and dV of half h of tile i - 1 has consumed the P^T there.
+      // The halves pipeline independently, which shortens the chain
+      // S^T -> P^T -> dV -> next S^T that a single buffer imposes.
+      constexpr uint32_t id_s = idesc_bf16(128, 64, 0, 0);
+      bool ok = mbar_spin(bar(B_KV_FULL), 0, w);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int qs = it % kStages;
+        if (!(ok = mbar_spin(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!(ok = mbar_spin(bar(B_S_FREE + hf), (it & 1) ^ 1, w))) break;
+          tc_fence_after();
+          const uint32_t bq = sb + OFF_Q + qs * kTile + hf * 64 * 128;  // query rows 64 hf ..
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + tm, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024), id_s,
-                    kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            umma_bf16(tmem + TM_ST + hf * 64, sdesc_sw128(sb + OFF_K + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024),
+                      id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(B_S_FULL + hf));
         }
-        umma_commit(bar(done));
-      };
-      bool ok = mbar_wait(bar(B_KV_FULL), 0, w);
-      int ns = 0, nd = 0;
-      Watchdog wd;
-      wd.reset();
-      while (ok && nd < n_it) {
-        bool did = false;
-        if (ns < n_it && s_ready(ns)) {
-          tc_fence_after();
-          issue_kq(ns, sb + OFF_K, sb + OFF_Q, TM_ST, B_S_FULL);
-          ++ns;
-          did = true;
-        }
-        if (nd < ns && dp_ready(nd)) {
-          tc_fence_after();
-          issue_kq(nd, sb + OFF_V, sb + OFF_DO, TM_DPT, B_DP_FULL);
-          ++nd;
-          did = true;
-        }
-        if (did) wd.reset();
-        else ok = wd.alive(w);
       }
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
-  } else if (warp == kGrad) {
+  } else if (warp == kDpMma) {
     if (lane == 0) {
-      // dV(i) += P^T(i) dO(i) once P^T is written (then the S^T columns are
-      // free), dK(i) += dS^T(i) Q(i) once dS^T is written (then the dP^T
-      // columns and the Q/dO stage are free: S^T(i) and dP^T(i) had completed
-      // before the compute warps could write P^T and dS^T).
-      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // A from TMEM, B MN-major
-      auto issue_grad = [&](int it, int tm_a, uint32_t b_base, int tm_d) {
-        const uint32_t bq = b_base + (it % kStages) * kTile;
+      // dP^T(i) = V dO(i)^T once the stage has landed and dK(i - 1) is done.
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+      bool ok = mbar_spin(bar(B_KV_FULL), 0, w);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int qs = it % kStages;
+        if (!(ok = mbar_spin(bar(B_QDO_FULL + qs), (it / kStages) & 1, w))) break;
+        if (!(ok = mbar_spin(bar(B_DP_FREE), (it & 1) ^ 1, w))) break;
+        tc_fence_after();
+        const uint32_t bq = sb + OFF_DO + qs * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + TM_DPT, sdesc_sw128(sb + OFF_V + off, 16, 1024), sdesc_sw128(bq + off, 16, 1024), id_s,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(B_DP_FULL));
+      }
+      umma_commit(bar(B_DRAIN_P));
+      mbar_wait_drain(bar(B_DRAIN_P), 0, p.status);
+    }
+  } else if (warp == kGrad) {
+    if (lane == 0) {
+      // dV(i) += P^T(i) dO(i) half by half as each half's P^T is written
+      // (then that half's S^T columns are free); dK(i) += dS^T(i) Q(i) once
+      // dS^T is written (then the dP^T columns and the Q/dO stage are free:
+      // S^T(i) and dP^T(i) had completed before the compute warps could write
+      // P^T and dS^T).
+      constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 1);  // A from TMEM, B MN-major
+      auto issue_grad = [&](int it, int tm_a, uint32_t b_base, int tm_d, int kk0, int kk1) {
+        const uint32_t bq = b_base + (it % kStages) * kTile;
+        for (int kk = kk0; kk < kk1; ++kk) {
           // queries 16 kk .. 16 kk + 15: compute group kk / 2 wrote them at
           // its own 32-column slice
           const uint32_t a = tmem + tm_a + (kk >> 1) * 32 + (kk & 1) * 8;
@@ -636,18 +634,16 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       bool ok = true;
       if (carry_in) ok = mbar_wait(bar(B_CARRY_READY), 0, w);
       for (int it = 0; ok && it < n_it; ++it) {
-        if (!(ok = mbar_spin(bar(B_P_FULL), it & 1, w))) break;
-        tc_fence_after();
-        issue_grad(it, TM_ST, sb + OFF_DO, TM_DV);
-        umma_commit(bar(B_S_FREE));
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!(ok = mbar_spin(bar(B_P_FULL + hf), it & 1, w))) break;
+          tc_fence_after();
+          issue_grad(it, TM_ST, sb + OFF_DO, TM_DV, 4 * hf, 4 * hf + 4);
+          umma_commit(bar(B_S_FREE + hf));
+        }
+        if (!ok) break;
         if (!(ok = mbar_spin(bar(B_DS_FULL), it & 1, w))) break;
-        // S^T of the next tile is on the critical path (P^T, then dV, wait
-        // for it); dK only gates dP^T of the next tile, which is needed later.
-        // So dK waits until S^T(it + 1) has landed rather than share the
-        // tensor pipe with it.
-        if (it + 1 < n_it && !(ok = mbar_spin(bar(B_S_FULL), (it + 1) & 1, w))) break;
         tc_fence_after();
-        issue_grad(it, TM_DPT, sb + OFF_Q, TM_DK);
+        issue_grad(it, TM_DPT, sb + OFF_Q, TM_DK, 0, 8);
         umma_commit(bar(B_DP_FREE));
         umma_commit(bar(B_QDO_EMPTY + it % kStages));
       }
@@ -698,22 +694,20 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       const int q0 = qt * 128 + grp * 32;  // query of this warp's first column
       // Without its record (all 64 queries past L) the slice is all zero.
       const bool live = 2 * qt + (grp >> 1) < n_q64;
-      // This warp's 32 queries in their record: -LSE*log2(e) at +0, Delta at +64.
+      // This warp's 32 queries in their record: -LSE*log2(e) at +0, Delta at
+      // +64.  Lane c loads query c's pair now, ahead of the waits, and the
+      // values reach the other lanes by shuffle.
       const float* rec = p.ld + (static_cast<int64_t>(hl) * n_q64 + 2 * qt + (grp >> 1)) * 128 + (grp & 1) * 32;
-      if (live) {
-        prefetch_l1(rec);
-        prefetch_l1(rec + 64);
-      }
+      const float nl = live ? __ldg(rec + lane) : 0.f;
+      const float dl = live ? __ldg(rec + 64 + lane) : 0.f;
       // ---- phase 1: P^T over the S^T columns, 16 at a time; the packed
       // P^T of columns 16 h .. 16 h + 15 goes to columns 8 h .. 8 h + 7, which
       // this warp has already read.
-      if (!(ok = warp_wait(bar(B_S_FULL), it & 1, w))) break;
+      if (!(ok = warp_wait(bar(B_S_FULL + (grp >> 1)), it & 1, w))) break;
       tc_fence_after();
       float pf[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float4 l4[4];
-        load_rec16(rec + 16 * h, live, l4);
         uint32_t sv[16];
         tmem_ld16(ts + 16 * h, sv);
         tmem_ld_wait(sv);
@@ -721,9 +715,9 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) pf[16 * h + c] = 0.f;
         } else if (qt == kb) {  // the diagonal tile (warp-uniform)
-          p_slice<true>(sv, l4, sl2, q0 + 16 * h, kpos, pf + 16 * h);
+          p_slice<true>(sv, nl, 16 * h, sl2, q0, kpos, pf + 16 * h);
         } else {
-          p_slice<false>(sv, l4, sl2, q0 + 16 * h, kpos, pf + 16 * h);
+          p_slice<false>(sv, nl, 16 * h, sl2, q0, kpos, pf + 16 * h);
         }
         uint32_t pk[8];
 #pragma unroll
@@ -733,14 +727,12 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      if (lane == 0) mbar_arrive(bar(B_P_FULL + (grp >> 1)));
       // ---- phase 2: dS^T = P^T * (dP^T - Delta) over the dP^T columns
       if (!(ok = warp_wait(bar(B_DP_FULL), it & 1, w))) break;
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float4 d4[4];
-        load_rec16(rec + 64 + 16 * h, live, d4);
         uint32_t dv[16];
         tmem_ld16(td + 16 * h, dv);
         tmem_ld_wait(dv);
@@ -749,7 +741,7 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) dd[c] = 0u;
         } else {
-          dst_slice(dv, pf + 16 * h, d4, dd);
+          dst_slice(dv, pf + 16 * h, dl, 16 * h, dd);
         }
         tmem_st8(td + 8 * h, dd);
       }

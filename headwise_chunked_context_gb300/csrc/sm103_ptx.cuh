@@ -199,11 +199,6 @@ struct Watchdog {
 
 // --------------------------------------------------------------------- TMA
 
-// Pulls the 128-byte line holding `p` into L1.
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
