@@ -8,13 +8,18 @@
 // into a carried partial result (same write-up, paragraph on intermediate
 // buffers: "a partial result is stored").
 //
-// Kernel shape: one CTA per 128x128 output tile, K in blocks of 64 bf16
-// (one 128-byte swizzle row), a 3-stage TMA ring, one thread issuing
-// tcgen05.mma (M=128, N=128, K=16) into a 128-column TMEM accumulator,
-// four epilogue warps reading the accumulator back one row per thread.
+// Kernel shape: persistent, one CTA per SM walking 128x256 output tiles
+// (two adjacent 128-column slots; a lone last slot makes an N=128 tile).
+// K goes in blocks of 64 bf16 (one 128-byte swizzle row) through a TMA ring
+// that runs across tile boundaries; one thread issues tcgen05.mma (M=128,
+// N=256, K=16) into one of two 256-column TMEM accumulators, and four
+// epilogue warps drain the other, so a tile's epilogue overlaps the next
+// tile's main loop.  N=256 halves the A reads per flop against N=128: with
+// both operands in shared memory the tensor core is bound by shared-memory
+// bandwidth (operand reads plus the TMA writes that fill the ring).
 // Operands are K-major (rows of 64 contiguous K) or MN-major (rows of
-// contiguous M/N, two 64-wide boxes per tile); both use the same swizzled
-// shared layout and differ only in the descriptor.
+// contiguous M/N, 64-wide boxes); both use the same swizzled shared layout
+// and differ only in the descriptor.
 //
 // Fixed reduction order: every output element accumulates its K blocks in
 // ascending order inside TMEM; a carried fp32 partial (out32 / dx32) is
@@ -34,22 +39,24 @@ constexpr int kTile = 128 * 64 * 2;  // one 16 KB operand tile (128 x 64 bf16)
 template <int KIND>
 struct Layout {
   static constexpr bool kSplit = (KIND == GK_DWQKV || KIND == GK_DX);
-  static constexpr int kStages = kSplit ? 2 : 3;
+  static constexpr int kStages = kSplit ? 3 : 4;
   static constexpr int kA = kSplit ? 2 * kTile : kTile;
-  static constexpr int kStage = kA + kTile;
+  static constexpr int kB = 2 * kTile;  // two 128-column slots
+  static constexpr int kStage = kA + kB;
   static constexpr int OFF_BAR = kStages * kStage;
   static constexpr int B_FULL = 0;
   static constexpr int B_EMPTY = kStages;
-  static constexpr int B_ACC_FULL = 2 * kStages;
-  static constexpr int B_ACC_READY = 2 * kStages + 1;
-  static constexpr int B_DRAIN = 2 * kStages + 2;
-  static constexpr int B_COUNT = 2 * kStages + 3;
+  static constexpr int B_ACC_FULL = 2 * kStages;      // per accumulator: products done
+  static constexpr int B_ACC_FREE = 2 * kStages + 2;  // per accumulator: drained (and carry loaded)
+  static constexpr int B_DRAIN = 2 * kStages + 4;
+  static constexpr int B_COUNT = 2 * kStages + 5;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 8;
   static constexpr int kSmemBytes = OFF_ABORT + 8 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "gemm shared memory");
 };
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 
 template <int KIND>
 struct Traits;
@@ -106,8 +113,126 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
   else return sdesc_sw128(base + kk * 32, 16, 1024);
 }
 
+// Writes one 128-column slot of a finished accumulator (TMEM row address
+// `trow`, one output row per thread) in the kind's output format.
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, int m, int r, int mt, int nt,
+                                           bool valid) {
+  constexpr bool kCarry = (KIND == GK_OPROJ || KIND == GK_DX);
+  if constexpr (KIND == GK_QKV) {
+    const int slot = nt;
+    __nv_bfloat16* orow =
+        static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
+    const bool rot = slot < p.rope_slots;
+    const float2* tab = p.rope + static_cast<int64_t>(m) * 64;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t a[32], b[32];
+      tmem_ld32(trow + half * 32, a);
+      tmem_ld32(trow + 64 + half * 32, b);
+      tmem_ld_wait(a);
+      tmem_ld_wait(b);
+      float lo[32], hi[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float x0 = __uint_as_float(a[i]);
+        const float x1 = __uint_as_float(b[i]);
+        if (rot && valid) {
+          const float2 cs = tab[half * 32 + i];
+          lo[i] = x0 * cs.x - x1 * cs.y;
+          hi[i] = x0 * cs.y + x1 * cs.x;
+        } else {
+          lo[i] = x0;
+          hi[i] = x1;
+        }
+      }
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          st_global_v4(orow + half * 32 + q * 8, pack_bf16x2(lo[8 * q], lo[8 * q + 1]),
+                       pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]), pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]),
+                       pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
+          st_global_v4(orow + 64 + half * 32 + q * 8, pack_bf16x2(hi[8 * q], hi[8 * q + 1]),
+                       pack_bf16x2(hi[8 * q + 2], hi[8 * q + 3]), pack_bf16x2(hi[8 * q + 4], hi[8 * q + 5]),
+                       pack_bf16x2(hi[8 * q + 6], hi[8 * q + 7]));
+        }
+      }
+    }
+  } else if constexpr (KIND == GK_DO) {
+    const int slot = nt;
+    __nv_bfloat16* orow =
+        static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
+    const __nv_bfloat16* obf = p.o_rows + static_cast<int64_t>(m) * p.ld_o + slot * kHeadDim;
+    float dsum = 0.f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t v[32];
+      tmem_ld32(trow + c4 * 32, v);
+      tmem_ld_wait(v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          st_global_v4(orow + c4 * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          const uint4 ov = ld_global_nc_v4(obf + c4 * 32 + q * 8);
+          const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dsum = fmaf(bf16_lo(pk[4 * q + e]), bf16_lo(ow[e]), dsum);
+            dsum = fmaf(bf16_hi(pk[4 * q + e]), bf16_hi(ow[e]), dsum);
+          }
+        }
+      }
+    }
+    // LSE/Delta record of this row (padding rows past L get -inf / 0).
+    const int n_q64 = (p.L + 63) / 64;
+    if (m < n_q64 * 64) {
+      float* rec = p.ld_rec + (static_cast<int64_t>(slot) * n_q64 + (m >> 6)) * 128;
+      rec[m & 63] = valid ? -p.lse_in[static_cast<int64_t>(slot) * p.L + m] * 1.4426950408889634074f : -INFINITY;
+      rec[64 + (m & 63)] = valid ? dsum : 0.f;
+    }
+  } else {
+    // fp32 or carried outputs: OPROJ, DX (carry / final bf16), DWO, DWQKV (fp32).
+    float* frow = nullptr;
+    __nv_bfloat16* brow = nullptr;
+    if constexpr (kCarry) {
+      if (p.final_out)
+        brow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(m) * p.ld_out + nt * 128;
+      else
+        frow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
+    } else if constexpr (KIND == GK_DWO) {
+      frow = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ld_out + p.out_col0 + nt * 128;
+    } else {  // GK_DWQKV
+      frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
+    }
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t v[32];
+      tmem_ld32(trow + c4 * 32, v);
+      tmem_ld_wait(v);
+      if (valid) {
+        if (brow) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_global_v4(brow + c4 * 32 + q * 8,
+                         pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
                 const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -117,12 +242,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int kStages = Lt::kStages;
   constexpr int OFF_BAR = Lt::OFF_BAR;
   constexpr int B_FULL = Lt::B_FULL, B_EMPTY = Lt::B_EMPTY, B_ACC_FULL = Lt::B_ACC_FULL;
-  constexpr int B_ACC_READY = Lt::B_ACC_READY, B_DRAIN = Lt::B_DRAIN;
+  constexpr int B_ACC_FREE = Lt::B_ACC_FREE, B_DRAIN = Lt::B_DRAIN;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // N tiles vary fastest so that CTAs resident together share the A row block.
-  const int nt = blockIdx.x;
-  const int mt = blockIdx.y;
+  // Tile t = (m tile t / n_pairs, slot pair t % n_pairs): consecutive CTAs
+  // share the A row block.
+  const int n_pairs = (p.n_tiles + 1) / 2;
+  const int total = p.m_tiles * n_pairs;
+  const int t0 = blockIdx.x;
+  const int G = gridDim.x;
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lt::OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
@@ -134,8 +262,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_ACC_FULL), 1);
-    mbar_init(bar(B_ACC_READY), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_ACC_FULL + b), 1);
+      mbar_init(bar(B_ACC_FREE + b), 4);
+    }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -157,15 +287,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       int last[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last[s] = -1;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1;
-        if (!mbar_wait(bar(B_EMPTY + s), ph ^ 1, w)) break;
-        const uint32_t dst = sb + s * Lt::kStage;
-        mbar_expect_tx(bar(B_FULL + s), Lt::kStage);
-        load_a<KIND>(&ma, p, dst, bar(B_FULL + s), mt, kb);
-        load_b<KIND>(&mb, p, dst + Lt::kA, bar(B_FULL + s), nt, kb);
-        last[s] = kb;
+      int g = 0;  // k blocks issued so far, across tiles
+      bool ok = true;
+      for (int t = t0; ok && t < total; t += G) {
+        const int mt = t / n_pairs;
+        const int nt0 = 2 * (t % n_pairs);
+        const bool two = nt0 + 1 < p.n_tiles;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!(ok = mbar_wait(bar(B_EMPTY + s), ((g / kStages) & 1) ^ 1, w))) break;
+          const uint32_t dst = sb + s * Lt::kStage;
+          mbar_expect_tx(bar(B_FULL + s), Lt::kA + (two ? 2 : 1) * kTile);
+          load_a<KIND>(&ma, p, dst, bar(B_FULL + s), mt, kb);
+          load_b<KIND>(&mb, p, dst + Lt::kA, bar(B_FULL + s), nt0, kb);
+          if (two) load_b<KIND>(&mb, p, dst + Lt::kA + kTile, bar(B_FULL + s), nt0 + 1, kb);
+          last[s] = g;
+        }
       }
       if (*abort_flag) {
         for (int s = 0; s < kStages; ++s)
@@ -175,33 +312,40 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 128, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
+      constexpr uint32_t id2 = idesc_bf16(128, 256, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
+      constexpr uint32_t id1 = idesc_bf16(128, 128, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
       bool ok = true;
-      if (carry_in) {
-        ok = mbar_wait(bar(B_ACC_READY), 0, w);
+      int g = 0;
+      int i = 0;
+      for (int t = t0; ok && t < total; t += G, ++i) {
+        const int b = i & 1;
+        const bool two = 2 * (t % n_pairs) + 1 < p.n_tiles;
+        const uint32_t idesc = two ? id2 : id1;
+        const uint32_t acc = tmem + b * 256;
+        if (!(ok = mbar_spin(bar(B_ACC_FREE + b), (i >> 1) & 1, w))) break;
         tc_fence_after();
-      }
-      for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1;
-        if (!(ok = mbar_wait(bar(B_FULL + s), ph, w))) break;
-        tc_fence_after();
-        const uint32_t a = sb + s * Lt::kStage;
-        const uint32_t b = a + Lt::kA;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!(ok = mbar_spin(bar(B_FULL + s), (g / kStages) & 1, w))) break;
+          tc_fence_after();
+          const uint32_t a = sb + s * Lt::kStage;
+          const uint32_t bb = a + Lt::kA;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(b, kk), idesc,
-                    (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
-        }
-        if constexpr (Lt::kSplit) {
+          for (int kk = 0; kk < 4; ++kk) {
+            umma_bf16(acc, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(bb, kk), idesc,
+                      (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (Lt::kSplit) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, operand_desc<Traits<KIND>::a_mn>(a + kTile, kk), operand_desc<Traits<KIND>::b_mn>(b, kk),
-                      idesc, 1u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(acc, operand_desc<Traits<KIND>::a_mn>(a + kTile, kk),
+                        operand_desc<Traits<KIND>::b_mn>(bb, kk), idesc, 1u);
+          }
+          umma_commit(bar(B_EMPTY + s));
         }
-        umma_commit(bar(B_EMPTY + s));
+        if (!ok) break;
+        umma_commit(bar(B_ACC_FULL + b));
       }
-      if (ok) umma_commit(bar(B_ACC_FULL));
       umma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
@@ -209,147 +353,58 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int m = mt * 128 + r;
-    const bool valid = m < p.M;
-    const uint32_t trow = tmem_lane_addr(tmem, quad, 0);
-    bool ok = true;
-
-    if constexpr (kCarry) {
-      if (carry_in) {
-        const float* crow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
+    const uint32_t trow0 = tmem_lane_addr(tmem, quad, 0);
+    // Makes accumulator (local tile li) & 1 ready for tile t: loads its
+    // carry when there is one, then releases it to the MMA thread.
+    auto prep = [&](int li, int t) {
+      if constexpr (kCarry) {
+        if (carry_in) {
+          const int m = (t / n_pairs) * 128 + r;
+          const bool valid = m < p.M;
+          const int nt0 = 2 * (t % n_pairs);
+          const int ns = nt0 + 1 < p.n_tiles ? 2 : 1;
+          for (int j = 0; j < ns; ++j) {
+            const float* crow = p.carry + static_cast<int64_t>(m) * p.N + (nt0 + j) * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint32_t v[32];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint4 t = valid ? ld_global_nc_v4(crow + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
-            v[4 * q] = t.x;
-            v[4 * q + 1] = t.y;
-            v[4 * q + 2] = t.z;
-            v[4 * q + 3] = t.w;
-          }
-          tmem_st32(trow + c4 * 32, v);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_ACC_READY));
-      }
-    }
-
-    ok = warp_wait(bar(B_ACC_FULL), 0, w);
-    if (ok) {
-      tc_fence_after();
-      if constexpr (KIND == GK_QKV) {
-        const int slot = nt;
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
-        const bool rot = slot < p.rope_slots;
-        const float2* tab = p.rope + static_cast<int64_t>(m) * 64;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32], b[32];
-          tmem_ld32(trow + half * 32, a);
-          tmem_ld32(trow + 64 + half * 32, b);
-          tmem_ld_wait(a);
-          tmem_ld_wait(b);
-          float lo[32], hi[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x0 = __uint_as_float(a[i]);
-            const float x1 = __uint_as_float(b[i]);
-            if (rot && valid) {
-              const float2 cs = tab[half * 32 + i];
-              lo[i] = x0 * cs.x - x1 * cs.y;
-              hi[i] = x0 * cs.y + x1 * cs.x;
-            } else {
-              lo[i] = x0;
-              hi[i] = x1;
-            }
-          }
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              st_global_v4(orow + half * 32 + q * 8, pack_bf16x2(lo[8 * q], lo[8 * q + 1]),
-                           pack_bf16x2(lo[8 * q + 2], lo[8 * q + 3]), pack_bf16x2(lo[8 * q + 4], lo[8 * q + 5]),
-                           pack_bf16x2(lo[8 * q + 6], lo[8 * q + 7]));
-              st_global_v4(orow + 64 + half * 32 + q * 8, pack_bf16x2(hi[8 * q], hi[8 * q + 1]),
-                           pack_bf16x2(hi[8 * q + 2], hi[8 * q + 3]), pack_bf16x2(hi[8 * q + 4], hi[8 * q + 5]),
-                           pack_bf16x2(hi[8 * q + 6], hi[8 * q + 7]));
-            }
-          }
-        }
-      } else if constexpr (KIND == GK_DO) {
-        const int slot = nt;
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(slot) * p.L + m) * kHeadDim;
-        const __nv_bfloat16* obf = p.o_rows + static_cast<int64_t>(m) * p.ld_o + slot * kHeadDim;
-        float dsum = 0.f;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(trow + c4 * 32, v);
-          tmem_ld_wait(v);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              st_global_v4(orow + c4 * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-              const uint4 ov = ld_global_nc_v4(obf + c4 * 32 + q * 8);
-              const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                dsum = fmaf(bf16_lo(pk[4 * q + e]), bf16_lo(ow[e]), dsum);
-                dsum = fmaf(bf16_hi(pk[4 * q + e]), bf16_hi(ow[e]), dsum);
+              for (int q = 0; q < 8; ++q) {
+                uint4 x = valid ? ld_global_nc_v4(crow + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
+                v[4 * q] = x.x;
+                v[4 * q + 1] = x.y;
+                v[4 * q + 2] = x.z;
+                v[4 * q + 3] = x.w;
               }
+              tmem_st32(trow0 + (li & 1) * 256 + j * 128 + c4 * 32, v);
             }
           }
-        }
-        // LSE/Delta record of this row (padding rows past L get -inf / 0).
-        const int n_q64 = (p.L + 63) / 64;
-        if (m < n_q64 * 64) {
-          float* rec = p.ld_rec + (static_cast<int64_t>(slot) * n_q64 + (m >> 6)) * 128;
-          rec[m & 63] = valid ? -p.lse_in[static_cast<int64_t>(slot) * p.L + m] * 1.4426950408889634074f : -INFINITY;
-          rec[64 + (m & 63)] = valid ? dsum : 0.f;
-        }
-      } else {
-        // fp32 or carried outputs: OPROJ, DX (carry / final bf16), DWO, DWQKV (fp32).
-        float* frow = nullptr;
-        __nv_bfloat16* brow = nullptr;
-        if constexpr (kCarry) {
-          if (p.final_out)
-            brow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(m) * p.ld_out + nt * 128;
-          else
-            frow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
-        } else if constexpr (KIND == GK_DWO) {
-          frow = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ld_out + p.out_col0 + nt * 128;
-        } else {  // GK_DWQKV
-          frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
-        }
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(trow + c4 * 32, v);
-          tmem_ld_wait(v);
-          if (valid) {
-            if (brow) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                st_global_v4(brow + c4 * 32 + q * 8,
-                             pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                             pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                             pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                             pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-            } else {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                st_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-          }
+          tmem_st_wait();
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACC_FREE + (li & 1)));
+    };
+    if (t0 < total) prep(0, t0);
+    if (t0 + G < total) prep(1, t0 + G);
+    bool ok = true;
+    int i = 0;
+    for (int t = t0; ok && t < total; t += G, ++i) {
+      const int b = i & 1;
+      const int mt = t / n_pairs;
+      const int nt0 = 2 * (t % n_pairs);
+      const int ns = nt0 + 1 < p.n_tiles ? 2 : 1;
+      const int m = mt * 128 + r;
+      const bool valid = m < p.M;
+      if (!(ok = warp_wait(bar(B_ACC_FULL + b), (i >> 1) & 1, w))) break;
+      tc_fence_after();
+      for (int j = 0; j < ns; ++j) {
+        const int nt = nt0 + j;
+        const uint32_t trow = trow0 + b * 256 + j * 128;
+        store_slot<KIND>(p, trow, m, r, mt, nt, valid);
+      }
+      if (t + 2 * G < total) prep(i + 2, t + 2 * G);
     }
     tc_fence_before();
   }
@@ -361,12 +416,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// Multiprocessor count of the current device (cached per device).
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  static int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 template <int KIND>
 cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t s) {
   constexpr int smem = Layout<KIND>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_tiles, p.m_tiles);
+  const int total = p.m_tiles * ((p.n_tiles + 1) / 2);
+  const int grid = total < sm_count() ? total : sm_count();  // persistent: one CTA per SM
+  if (grid <= 0) return cudaSuccess;
   gemm_kernel<KIND><<<grid, kThreads, smem, s>>>(a, b, p);
   return cudaGetLastError();
 }
