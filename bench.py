@@ -201,9 +201,13 @@ def run_reference(args, w, world, rank):
 
 
 def source_sha(name):
-    p = os.path.join(ROOT, "headwise_chunked_context_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file together with the headers every kernel
+    includes, so that a change to either invalidates a stored capture."""
+    h = hashlib.sha256()
+    for f in (name, "sm103_ptx.cuh", "upipe_internal.h"):
+        with open(os.path.join(ROOT, "headwise_chunked_context_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 KIND_SOURCE = {"attn_fwd": "attn_fwd.cu", "attn_bwd_dq": "attn_bwd.cu", "attn_bwd_dkdv": "attn_bwd.cu"}
