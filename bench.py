@@ -298,8 +298,30 @@ def run_upipe(args, w, world, rank, local):
     ms = max_over_ranks(ms, dev)
     peak_alloc = torch.cuda.max_memory_allocated(dev) - base_alloc
 
+    # ---- forward and backward timed separately, after the step timing
+    def timed(fn, n):
+        fn()
+        torch.cuda.synchronize(dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        return a0.elapsed_time(a1) / n
+    n_split = max(1, min(args.steps, 3))
+    fwd_ms = timed(lambda: upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream), n_split)
+    bwd_ms = timed(lambda: upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream), n_split)
+    code = upipe.last_device_status(stream)
+    if code != 0:
+        raise RuntimeError(f"device status after the fwd/bwd split: {upipe.strerror(code)}")
+
     attn_f, proj_f = layer_flops(L, D, H, Hkv)
     step_flops = attn_f + proj_f
+    # Hardware work adds the backward's recompute of the QKV slices and of the
+    # attention forward (the forward's share of attn_f is 2 of its 7 parts).
+    recompute_flops = attn_f * 2.0 / 7.0 + 2.0 * L * D * (H + 2 * Hkv) * 128
     ms_step = ms / args.steps
     value = job_tflops(step_flops, ms_step, world)
     burst, sustained, hbm, peak_src = peaks()
@@ -386,6 +408,11 @@ def run_upipe(args, w, world, rank, local):
                           "peaks": f"{burst}/{sustained} TFLOP/s ({peak_src})"},
         "attn_core_tflops": world * attn_f / (sum(busy[k][0] for k in ("attn_fwd", "attn_bwd_dq", "attn_bwd_dkdv")
                                                   if k in busy) / args.steps / 1e3) / 1e12,
+        "fwd_bwd": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                    "fwd_tflops": world * (attn_f * 2.0 / 7.0 + proj_f / 3.0) / (fwd_ms / 1e3) / 1e12,
+                    "bwd_tflops": world * (attn_f * 5.0 / 7.0 + proj_f * 2.0 / 3.0) / (bwd_ms / 1e3) / 1e12},
+        "hfu": {"value": world * (step_flops + recompute_flops) / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
+                "note": "hardware flops: the layer flops plus the backward's recompute of QKV and attention fwd"},
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clocks, "activation_bytes": act, "peak_alloc_bytes_in_step": peak_alloc,
     }

@@ -8,15 +8,22 @@
 // into a carried partial result (same write-up, paragraph on intermediate
 // buffers: "a partial result is stored").
 //
-// Kernel shape: persistent, one CTA per SM walking 128x256 output tiles
-// (two adjacent 128-column slots; a lone last slot makes an N=128 tile).
+// Kernel shape: persistent CTA pairs (clusters of two, one CTA per SM)
+// walking 256x256 output tiles.  CTA r of a pair owns the 128 rows of m
+// tile 2 mp + r and loads B slot 2 np + r; the even CTA's thread issues
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which takes A and B from
+// both CTAs' shared memory and leaves each CTA its own 128 rows of D in its
+// TMEM.  Per SM that is one 128x256x16 product per 4 KB of A and 4 KB of B
+// read from (and written by TMA into) shared memory, against 12 KB for a
+// single-CTA 128x256 product: with both operands in shared memory a single
+// CTA is bound by shared-memory bandwidth, a pair reaches the tensor rate.
 // K goes in blocks of 64 bf16 (one 128-byte swizzle row) through a TMA ring
-// that runs across tile boundaries; one thread issues tcgen05.mma (M=128,
-// N=256, K=16) into one of two 256-column TMEM accumulators, and four
-// epilogue warps drain the other, so a tile's epilogue overlaps the next
-// tile's main loop.  N=256 halves the A reads per flop against N=128: with
-// both operands in shared memory the tensor core is bound by shared-memory
-// bandwidth (operand reads plus the TMA writes that fill the ring).
+// that runs across tile boundaries; both CTAs' copies of a stage complete
+// directly on the even CTA's barrier (cta_group::2 copies; a software
+// forwarding hop from the odd CTA cost ~900 cycles per stage).  D goes into
+// one of two 256-column
+// TMEM accumulators while the four epilogue warps of each CTA drain the
+// other, so a tile's epilogue overlaps the next tile's main loop.
 // Operands are K-major (rows of 64 contiguous K) or MN-major (rows of
 // contiguous M/N, 64-wide boxes); both use the same swizzled shared layout
 // and differ only in the descriptor.
@@ -39,15 +46,15 @@ constexpr int kTile = 128 * 64 * 2;  // one 16 KB operand tile (128 x 64 bf16)
 template <int KIND>
 struct Layout {
   static constexpr bool kSplit = (KIND == GK_DWQKV || KIND == GK_DX);
-  static constexpr int kStages = kSplit ? 3 : 4;
+  static constexpr int kStages = kSplit ? 4 : 6;
   static constexpr int kA = kSplit ? 2 * kTile : kTile;
-  static constexpr int kB = 2 * kTile;  // two 128-column slots
+  static constexpr int kB = kTile;  // this CTA's 128-column slot of the pair's 256
   static constexpr int kStage = kA + kB;
   static constexpr int OFF_BAR = kStages * kStage;
-  static constexpr int B_FULL = 0;
-  static constexpr int B_EMPTY = kStages;
+  static constexpr int B_FULL = 0;                    // even CTA: both CTAs' copies of the stage landed
+  static constexpr int B_EMPTY = kStages;             // the pair's products read the stage
   static constexpr int B_ACC_FULL = 2 * kStages;      // per accumulator: products done
-  static constexpr int B_ACC_FREE = 2 * kStages + 2;  // per accumulator: drained (and carry loaded)
+  static constexpr int B_ACC_FREE = 2 * kStages + 2;  // even CTA, per accumulator: both CTAs drained it
   static constexpr int B_DRAIN = 2 * kStages + 4;
   static constexpr int B_COUNT = 2 * kStages + 5;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
@@ -67,26 +74,27 @@ template <> struct Traits<GK_DWO>   { static constexpr int a_mn = 1, b_mn = 1; }
 template <> struct Traits<GK_DWQKV> { static constexpr int a_mn = 1, b_mn = 1; };
 template <> struct Traits<GK_DX>    { static constexpr int a_mn = 0, b_mn = 1; };
 
+// `bar` is the shared::cluster address of the even CTA's stage barrier.
 template <int KIND>
 __device__ __forceinline__ void load_a(const CUtensorMap* m, const GemmParams& p, uint32_t dst, uint32_t bar,
                                        int mt, int kb) {
   if constexpr (KIND == GK_QKV || KIND == GK_DO) {
-    tma_load_2d(dst, m, bar, kb * 64, mt * 128);
+    tma_load_2d_pair(dst, m, bar, kb * 64, mt * 128);
   } else if constexpr (KIND == GK_OPROJ) {
-    tma_load_2d(dst, m, bar, p.a_col0 + kb * 64, mt * 128);
+    tma_load_2d_pair(dst, m, bar, p.a_col0 + kb * 64, mt * 128);
   } else if constexpr (KIND == GK_DWO) {
-    tma_load_2d(dst, m, bar, mt * 128, kb * 64);
-    tma_load_2d(dst + 8192, m, bar, mt * 128 + 64, kb * 64);
+    tma_load_2d_pair(dst, m, bar, mt * 128, kb * 64);
+    tma_load_2d_pair(dst + 8192, m, bar, mt * 128 + 64, kb * 64);
   } else if constexpr (KIND == GK_DWQKV) {
     const int z = p.tab0[mt];
-    tma_load_3d(dst, m, bar, 0, kb * 64, z);
-    tma_load_3d(dst + 8192, m, bar, 64, kb * 64, z);
-    tma_load_3d(dst + kTile, m, bar, 0, kb * 64, z + p.lo_z);
-    tma_load_3d(dst + kTile + 8192, m, bar, 64, kb * 64, z + p.lo_z);
+    tma_load_3d_pair(dst, m, bar, 0, kb * 64, z);
+    tma_load_3d_pair(dst + 8192, m, bar, 64, kb * 64, z);
+    tma_load_3d_pair(dst + kTile, m, bar, 0, kb * 64, z + p.lo_z);
+    tma_load_3d_pair(dst + kTile + 8192, m, bar, 64, kb * 64, z + p.lo_z);
   } else {  // GK_DX
     const int z = p.tab0[kb >> 1];
-    tma_load_3d(dst, m, bar, (kb & 1) * 64, mt * 128, z);
-    tma_load_3d(dst + kTile, m, bar, (kb & 1) * 64, mt * 128, z + p.lo_z);
+    tma_load_3d_pair(dst, m, bar, (kb & 1) * 64, mt * 128, z);
+    tma_load_3d_pair(dst + kTile, m, bar, (kb & 1) * 64, mt * 128, z + p.lo_z);
   }
 }
 
@@ -94,16 +102,16 @@ template <int KIND>
 __device__ __forceinline__ void load_b(const CUtensorMap* m, const GemmParams& p, uint32_t dst, uint32_t bar,
                                        int nt, int kb) {
   if constexpr (KIND == GK_QKV) {
-    tma_load_2d(dst, m, bar, kb * 64, p.tab0[nt] * 128);
+    tma_load_2d_pair(dst, m, bar, kb * 64, p.tab0[nt] * 128);
   } else if constexpr (KIND == GK_OPROJ) {
-    tma_load_2d(dst, m, bar, p.b_col0 + kb * 64, nt * 128);
+    tma_load_2d_pair(dst, m, bar, p.b_col0 + kb * 64, nt * 128);
   } else if constexpr (KIND == GK_DO || KIND == GK_DWO || KIND == GK_DWQKV) {
-    tma_load_2d(dst, m, bar, p.b_col0 + nt * 128, kb * 64);
-    tma_load_2d(dst + 8192, m, bar, p.b_col0 + nt * 128 + 64, kb * 64);
+    tma_load_2d_pair(dst, m, bar, p.b_col0 + nt * 128, kb * 64);
+    tma_load_2d_pair(dst + 8192, m, bar, p.b_col0 + nt * 128 + 64, kb * 64);
   } else {  // GK_DX
     const int row = p.tab1[kb >> 1] * 128 + (kb & 1) * 64;
-    tma_load_2d(dst, m, bar, nt * 128, row);
-    tma_load_2d(dst + 8192, m, bar, nt * 128 + 64, row);
+    tma_load_2d_pair(dst, m, bar, nt * 128, row);
+    tma_load_2d_pair(dst + 8192, m, bar, nt * 128 + 64, row);
   }
 }
 
@@ -232,7 +240,7 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
                 const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -241,16 +249,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lt = Layout<KIND>;
   constexpr int kStages = Lt::kStages;
   constexpr int OFF_BAR = Lt::OFF_BAR;
-  constexpr int B_FULL = Lt::B_FULL, B_EMPTY = Lt::B_EMPTY, B_ACC_FULL = Lt::B_ACC_FULL;
-  constexpr int B_ACC_FREE = Lt::B_ACC_FREE, B_DRAIN = Lt::B_DRAIN;
+  constexpr int B_FULL = Lt::B_FULL, B_EMPTY = Lt::B_EMPTY;
+  constexpr int B_ACC_FULL = Lt::B_ACC_FULL, B_ACC_FREE = Lt::B_ACC_FREE, B_DRAIN = Lt::B_DRAIN;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Tile t = (m tile t / n_pairs, slot pair t % n_pairs): consecutive CTAs
-  // share the A row block.
+  const uint32_t rank = cluster_rank();
+  const bool even = rank == 0;
+  // Pair tile t = (m pair t / n_pairs, slot pair t % n_pairs): consecutive
+  // pairs share the A row block.
+  const int m_pairs = (p.m_tiles + 1) / 2;
   const int n_pairs = (p.n_tiles + 1) / 2;
-  const int total = p.m_tiles * n_pairs;
-  const int t0 = blockIdx.x;
-  const int G = gridDim.x;
+  const int total = m_pairs * n_pairs;
+  const int t0 = blockIdx.x >> 1;
+  const int G = gridDim.x >> 1;
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lt::OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
@@ -259,23 +270,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_FULL + s), 2);  // one expect_tx arrival from each CTA's producer
       mbar_init(bar(B_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_ACC_FULL + b), 1);
-      mbar_init(bar(B_ACC_FREE + b), 4);
+      mbar_init(bar(B_ACC_FREE + b), 8);  // 4 epilogue warps in each CTA
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + Lt::OFF_TMEM_SLOT, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(sb + Lt::OFF_TMEM_SLOT, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lt::OFF_TMEM_SLOT);
 
@@ -290,63 +302,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // k blocks issued so far, across tiles
       bool ok = true;
       for (int t = t0; ok && t < total; t += G) {
-        const int mt = t / n_pairs;
-        const int nt0 = 2 * (t % n_pairs);
-        const bool two = nt0 + 1 < p.n_tiles;
+        const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
+        const int mt_ld = mt < p.m_tiles ? mt : p.m_tiles - 1;  // a missing m tile reloads the last (unused)
+        const int ns = 2 * (t % n_pairs) + static_cast<int>(rank);
+        const bool has_b = ns < p.n_tiles;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
           const int s = g % kStages;
-          if (!(ok = mbar_wait(bar(B_EMPTY + s), ((g / kStages) & 1) ^ 1, w))) break;
+          // Polled: the arrival comes from the even CTA's commit, and a
+          // suspended try_wait was measured to wake late for it.
+          if (!(ok = mbar_spin<true>(bar(B_EMPTY + s), ((g / kStages) & 1) ^ 1, w))) break;
           const uint32_t dst = sb + s * Lt::kStage;
-          mbar_expect_tx(bar(B_FULL + s), Lt::kA + (two ? 2 : 1) * kTile);
-          load_a<KIND>(&ma, p, dst, bar(B_FULL + s), mt, kb);
-          load_b<KIND>(&mb, p, dst + Lt::kA, bar(B_FULL + s), nt0, kb);
-          if (two) load_b<KIND>(&mb, p, dst + Lt::kA + kTile, bar(B_FULL + s), nt0 + 1, kb);
+          const uint32_t full = mapa_shared(bar(B_FULL + s), 0);
+          mbar_expect_tx_cluster(full, Lt::kA + (has_b ? kTile : 0));
+          load_a<KIND>(&ma, p, dst, full, mt_ld, kb);
+          if (has_b) load_b<KIND>(&mb, p, dst + Lt::kA, full, ns, kb);
           last[s] = g;
         }
       }
-      if (*abort_flag) {
+      // Unwinding: every copy of either CTA completes on the even CTA's
+      // barriers, so the even CTA waits (bounded) for the stages issued last;
+      // the odd CTA stays resident until then (final cluster barrier).  A
+      // phase the other CTA never joined does not complete; its 1 s drain
+      // limit is far beyond any copy's flight time.
+      if (*abort_flag && even) {
         for (int s = 0; s < kStages; ++s)
-          if (last[s] >= 0) mbar_wait_drain(bar(B_FULL + s), (last[s] / kStages) & 1, p.status);
+          if (last[s] >= 0) mbar_wait_drain<true>(bar(B_FULL + s), (last[s] / kStages) & 1, p.status);
       }
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t id2 = idesc_bf16(128, 256, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
-      constexpr uint32_t id1 = idesc_bf16(128, 128, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
+    if (even && lane == 0) {
+      // ------------------------------------------- even CTA: pair products
+      constexpr uint32_t idesc = idesc_bf16(256, 256, Traits<KIND>::a_mn, Traits<KIND>::b_mn);
       bool ok = true;
       int g = 0;
       int i = 0;
       for (int t = t0; ok && t < total; t += G, ++i) {
         const int b = i & 1;
-        const bool two = 2 * (t % n_pairs) + 1 < p.n_tiles;
-        const uint32_t idesc = two ? id2 : id1;
         const uint32_t acc = tmem + b * 256;
-        if (!(ok = mbar_spin(bar(B_ACC_FREE + b), (i >> 1) & 1, w))) break;
+        if (!(ok = mbar_spin<true>(bar(B_ACC_FREE + b), (i >> 1) & 1, w))) break;
         tc_fence_after();
         for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
           const int s = g % kStages;
-          if (!(ok = mbar_spin(bar(B_FULL + s), (g / kStages) & 1, w))) break;
+          if (!(ok = mbar_spin<true>(bar(B_FULL + s), (g / kStages) & 1, w))) break;
           tc_fence_after();
           const uint32_t a = sb + s * Lt::kStage;
           const uint32_t bb = a + Lt::kA;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            umma_bf16(acc, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(bb, kk), idesc,
-                      (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_pair(acc, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(bb, kk),
+                           idesc, (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (Lt::kSplit) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(acc, operand_desc<Traits<KIND>::a_mn>(a + kTile, kk),
-                        operand_desc<Traits<KIND>::b_mn>(bb, kk), idesc, 1u);
+              umma_bf16_pair(acc, operand_desc<Traits<KIND>::a_mn>(a + kTile, kk),
+                             operand_desc<Traits<KIND>::b_mn>(bb, kk), idesc, 1u);
           }
-          umma_commit(bar(B_EMPTY + s));
+          umma_commit_pair(bar(B_EMPTY + s), 0x3);
         }
         if (!ok) break;
-        umma_commit(bar(B_ACC_FULL + b));
+        umma_commit_pair(bar(B_ACC_FULL + b), 0x3);
       }
-      umma_commit(bar(B_DRAIN));
+      umma_commit_pair(bar(B_DRAIN), 0x1);
       mbar_wait_drain(bar(B_DRAIN), 0, p.status);
     }
   } else {
@@ -354,17 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t trow0 = tmem_lane_addr(tmem, quad, 0);
-    // Makes accumulator (local tile li) & 1 ready for tile t: loads its
-    // carry when there is one, then releases it to the MMA thread.
+    const uint32_t acc_free_even = mapa_shared(bar(B_ACC_FREE), 0);
+    // Makes accumulator (local tile li) & 1 ready for pair tile t: loads this
+    // CTA's rows of the carry when there is one, then tells the even CTA.
     auto prep = [&](int li, int t) {
       if constexpr (kCarry) {
         if (carry_in) {
-          const int m = (t / n_pairs) * 128 + r;
-          const bool valid = m < p.M;
+          const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
+          const int m = mt * 128 + r;
+          const bool valid = mt < p.m_tiles && m < p.M;
           const int nt0 = 2 * (t % n_pairs);
-          const int ns = nt0 + 1 < p.n_tiles ? 2 : 1;
-          for (int j = 0; j < ns; ++j) {
-            const float* crow = p.carry + static_cast<int64_t>(m) * p.N + (nt0 + j) * 128;
+          const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
+          for (int j = 0; j < nsl; ++j) {
+            const float* crow = p.carry + static_cast<int64_t>(valid ? m : 0) * p.N + (nt0 + j) * 128;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               uint32_t v[32];
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_ACC_FREE + (li & 1)));
+      if (lane == 0) mbar_arrive_cluster(acc_free_even + 8 * (li & 1));
     };
     if (t0 < total) prep(0, t0);
     if (t0 + G < total) prep(1, t0 + G);
@@ -392,17 +411,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int i = 0;
     for (int t = t0; ok && t < total; t += G, ++i) {
       const int b = i & 1;
-      const int mt = t / n_pairs;
+      const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
       const int nt0 = 2 * (t % n_pairs);
-      const int ns = nt0 + 1 < p.n_tiles ? 2 : 1;
+      const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
       const int m = mt * 128 + r;
-      const bool valid = m < p.M;
-      if (!(ok = warp_wait(bar(B_ACC_FULL + b), (i >> 1) & 1, w))) break;
+      const bool tile_ok = mt < p.m_tiles;
+      const bool valid = tile_ok && m < p.M;
+      if (!(ok = warp_wait<true>(bar(B_ACC_FULL + b), (i >> 1) & 1, w))) break;
       tc_fence_after();
-      for (int j = 0; j < ns; ++j) {
-        const int nt = nt0 + j;
-        const uint32_t trow = trow0 + b * 256 + j * 128;
-        store_slot<KIND>(p, trow, m, r, mt, nt, valid);
+      if (tile_ok) {
+        for (int j = 0; j < nsl; ++j) {
+          const uint32_t trow = trow0 + b * 256 + j * 128;
+          store_slot<KIND>(p, trow, m, r, mt, nt0 + j, valid);
+        }
       }
       if (t + 2 * G < total) prep(i + 2, t + 2 * G);
     }
@@ -410,9 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  cluster_sync();  // the even CTA's products are drained; nothing in flight crosses CTAs
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -433,10 +455,35 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
   constexpr int smem = Layout<KIND>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int total = p.m_tiles * ((p.n_tiles + 1) / 2);
-  const int grid = total < sm_count() ? total : sm_count();  // persistent: one CTA per SM
-  if (grid <= 0) return cudaSuccess;
-  gemm_kernel<KIND><<<grid, kThreads, smem, s>>>(a, b, p);
+  // Persistent: as many pairs as can be resident at once.  A pair must fit
+  // inside one GPC, so that is fewer than SMs / 2 when GPCs have odd SM
+  // counts; more pairs than that would run as a second wave.
+  static int resident[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count()), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND>, &cfg);
+    if (e != cudaSuccess) return e;
+    resident[dev] = n > 0 ? n : 1;
+  }
+  const int total = ((p.m_tiles + 1) / 2) * ((p.n_tiles + 1) / 2);
+  const int pairs = total < resident[dev] ? total : resident[dev];
+  if (pairs <= 0) return cudaSuccess;
+  gemm_kernel<KIND><<<2 * pairs, kThreads, smem, s>>>(a, b, p);
   return cudaGetLastError();
 }
 

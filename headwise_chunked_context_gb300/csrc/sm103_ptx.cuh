@@ -59,30 +59,54 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
       : "memory");
 }
 
+// kCluster: acquire at cluster scope, for phases completed by arrivals or
+// copies from the other CTA of a pair.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Non-blocking probe: true iff the phase of parity `parity` has completed.
 // (try_wait may suspend the thread for a while; a thread that polls several
 // barriers and issues whichever is ready must not block on any one of them.)
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -97,11 +121,12 @@ struct WaitCtl {
 // Waits for the phase of parity `parity` of barrier `bar`.  Returns false if
 // the wait gave up: its own limit ran out (this thread then raises the abort
 // flag and records a timeout) or another thread of the CTA aborted first.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = sm_cycles();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if (*w.abort_flag) return false;
     if (sm_cycles() - t0 > w.limit_ns * kCyclesPerNs) {
       *w.abort_flag = 1;
@@ -114,10 +139,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // Bounded wait that spins on the non-blocking probe instead of try_wait, for
 // a thread whose next action is latency-critical (an MMA issuer): no
 // suspend/wake-up between the phase completing and the thread noticing.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test<kCluster>(bar, parity)) return true;
     if ((i & 31) != 0) continue;  // the abort flag and the clock every 32 polls
     if (*w.abort_flag) return false;
     const uint64_t now = sm_cycles();
@@ -134,9 +160,10 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, const W
 // Drain wait used while unwinding: ignores the abort flag, bounded by a fixed
 // limit.  Used only on events that complete without help from other threads
 // (TMA bytes landing, issued MMAs retiring).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = sm_cycles();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait<kCluster>(bar, parity)) {
     if (sm_cycles() - t0 > 1000000000ull * kCyclesPerNs) {
       atomicOr(status, UPIPE_STATUS_DRAIN_TIMEOUT);
       return false;
@@ -152,10 +179,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // ago, against about 15 for one warp-wide probe.  The abort flag and the
 // clock are checked every 32 rounds, by warp vote.  Must be called by all 32
 // lanes; the result is warp-uniform.
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_test<kCluster>(bar, parity))) return true;
     if ((i & 31) != 0) continue;
     if (__any_sync(0xffffffffu, *w.abort_flag != 0)) return false;
     const uint64_t now = sm_cycles();
@@ -247,6 +275,71 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+
+// ------------------------------------------------------ CTA pairs (cluster of 2)
+//
+// A pair of CTAs on two SMs runs one M=256 product: the even CTA's thread
+// issues tcgen05.mma.cta_group::2, each CTA supplies 128 rows of A and half
+// of B's N from its own shared memory at the same offsets, and each CTA's
+// TMEM receives its own 128 rows of D.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of both CTAs; used only where every thread arrives promptly
+// (after barrier initialisation, and at exit once every bounded wait has
+// returned).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Posts the byte count of copies that will complete on `cluster_bar`.
+// Relaxed: it publishes no data of this thread (the copies' completion is
+// tracked by the barrier's transaction count); a release here would wait
+// for this thread's earlier copies and serialise the ring.
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Tile copies into this CTA's shared memory that complete on a barrier of
+// either CTA of the pair (`cluster_bar`, a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(map), "r"(cluster_bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
+                                                 int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -275,6 +368,25 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A * B^T over a CTA pair (M = 256); issued by the even CTA.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on the barrier at offset `bar` in every CTA of `mask` when
+// every pair product issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 
