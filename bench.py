@@ -354,17 +354,33 @@ def run_upipe(args, w, world, rank, local):
         d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdx, hdw, hdwo))
         k_e2e = max(1, min(args.steps, 3))
 
+        # Copies that the layer does not wait for run on a second stream:
+        # dout streams in during the forward, out and LSE stream back during
+        # the backward.  Every byte still crosses inside the timed region.
+        cstream = torch.cuda.Stream(dev)
+        ev = [torch.cuda.Event() for _ in range(3)]
+
         def e2e_step():
             x.copy_(hx, non_blocking=True)
             wqkv.copy_(hw, non_blocking=True)
             wo.copy_(hwo, non_blocking=True)
-            dout.copy_(hd, non_blocking=True)
-            step()
-            ho.copy_(out, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            ev[0].record(stream)
+            cstream.wait_event(ev[0])                 # dout's buffer is free (previous bwd done)
+            with torch.cuda.stream(cstream):
+                dout.copy_(hd, non_blocking=True)
+                ev[1].record(cstream)
+            upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
+            ev[2].record(stream)
+            stream.wait_event(ev[1])                  # dout landed
+            upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream)
+            cstream.wait_event(ev[2])                 # out and LSE final
+            with torch.cuda.stream(cstream):
+                ho.copy_(out, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
             hdx.copy_(dx, non_blocking=True)
             hdw.copy_(dwqkv, non_blocking=True)
             hdwo.copy_(dwo, non_blocking=True)
+            stream.wait_stream(cstream)               # the step ends when every copy has landed
 
         e2e_step()
         torch.cuda.synchronize(dev)
