@@ -276,6 +276,19 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Register reallocation between warpgroups (all 128 threads of the
+// warpgroup execute it): dec gives registers back to the block's pool, inc
+// waits until the pool has them.  Callers check that the warpgroups' final
+// counts add up to no more than the block was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------ CTA pairs (cluster of 2)
 //
 // A pair of CTAs on two SMs runs one M=256 product: the even CTA's thread
