@@ -163,8 +163,10 @@ __global__ void __launch_bounds__(dq::kThreadsDq, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // most KV blocks first
-  const int h = blockIdx.y;
+  // Heads vary fastest (GQA siblings share K/V blocks in L2); the query
+  // blocks with the most KV blocks launch first.
+  const int h = static_cast<int>(blockIdx.x) % p.nheads;
+  const int qb = static_cast<int>(gridDim.x) / p.nheads - 1 - static_cast<int>(blockIdx.x) / p.nheads;
   const int kz = p.k_z0 + h / p.g_loc;
   const int vz = p.v_z0 + h / p.g_loc;
   const int n_kv = qb + 1;  // causal: 128-key blocks 0 .. qb
@@ -488,8 +490,10 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kb = blockIdx.x;  // key tile 0 sees every query: the heaviest tiles launch first
-  const int kv = blockIdx.y;
+  // Key tile 0 sees every query: the heaviest tiles launch first, KV heads
+  // varying fastest.
+  const int kb = static_cast<int>(blockIdx.x) / p.nkv;
+  const int kv = static_cast<int>(blockIdx.x) % p.nkv;
   const int n_q64 = (p.L + 63) / 64;
   const int n_q128 = (p.L + 127) / 128;
   const int nqt = n_q128 - kb;  // query tiles at or after this key tile
@@ -835,7 +839,7 @@ cudaError_t launch_attn_bwd_dq(const CUtensorMap& q, const CUtensorMap& k, const
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(n_qblocks, p.nheads);
+  dim3 grid(n_qblocks * p.nheads);
   attn_bwd_dq_kernel<<<grid, dq::kThreadsDq, dq::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }
@@ -845,7 +849,7 @@ cudaError_t launch_attn_bwd_dkdv(const CUtensorMap& q, const CUtensorMap& k, con
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(n_kblocks, p.nkv);
+  dim3 grid(n_kblocks * p.nkv);
   attn_bwd_dkdv_kernel<<<grid, dkv::kThreadsKv, dkv::kSmemBytes, s>>>(q, k, v, dO, p);
   return cudaGetLastError();
 }

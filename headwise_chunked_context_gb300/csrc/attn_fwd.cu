@@ -71,8 +71,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // heaviest tiles first
-  const int h = blockIdx.y;
+  // Heads vary fastest: the CTAs in flight hold the same query blocks of
+  // every head, whose K/V blocks (shared within a GQA group) stay in L2, and
+  // the query blocks with the most KV blocks launch first.
+  const int h = static_cast<int>(blockIdx.x) % p.nheads;
+  const int qb = static_cast<int>(gridDim.x) / p.nheads - 1 - static_cast<int>(blockIdx.x) / p.nheads;
   const int kz = p.k_z0 + h / p.g_loc;
   const int vz = p.v_z0 + h / p.g_loc;
   const int n_kv = qb + 1;  // causal: KV blocks 0..qb
@@ -360,7 +363,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const AttnFwdParams& p, int n_qblocks, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(n_qblocks, p.nheads);
+  dim3 grid(n_qblocks * p.nheads);
   attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(q, k, v, p);
   return cudaGetLastError();
 }

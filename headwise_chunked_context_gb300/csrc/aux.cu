@@ -86,7 +86,33 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
   }
 }
 
+struct ZeroRows {
+  float* base;
+  int64_t ld;
+  int cols;
+  int16_t blocks[kMaxSlots];
+};
+
+// One CTA per row: row (blockIdx.x & 127) of listed block blockIdx.x >> 7.
+__global__ void __launch_bounds__(256) zero_rows_kernel(const __grid_constant__ ZeroRows z) {
+  const int row = static_cast<int>(blockIdx.x);
+  float4* dst = reinterpret_cast<float4*>(z.base + (static_cast<int64_t>(z.blocks[row >> 7]) * 128 + (row & 127)) * z.ld);
+  for (int i = threadIdx.x; i < z.cols / 4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace
+
+cudaError_t launch_zero_rows(float* base, int64_t ld, int cols, const int16_t* blocks, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (n > kMaxSlots || cols % 4 != 0 || ld % 4 != 0) return cudaErrorInvalidValue;
+  ZeroRows z = {};
+  z.base = base;
+  z.ld = ld;
+  z.cols = cols;
+  for (int i = 0; i < n; ++i) z.blocks[i] = blocks[i];
+  zero_rows_kernel<<<static_cast<unsigned>(n * 128), 256, 0, s>>>(z);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_table(float2* table, int64_t L, double theta, cudaStream_t s) {
   RopeFreqs f;

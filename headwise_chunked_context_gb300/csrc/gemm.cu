@@ -32,6 +32,13 @@
 // ascending order inside TMEM; a carried fp32 partial (out32 / dx32) is
 // loaded into TMEM before the first MMA so that chunked and unchunked runs
 // perform the same fp32 additions in the same order.
+//
+// dWqkv (K = L tokens, only (U + 2 Hkv_c) / 2 x D / 256 pair tiles: 96 for
+// the 8B layer at U = 8, 1.26 waves of 76 pairs) splits K at k_mid into two
+// work units per tile, each reduced (red.global.add.f32) into the zeroed
+// output: 192 units fill the pairs 2.5 times instead of 1.26.  Two addends
+// into a zero give the same bits in either order, and k_mid depends only on
+// L, so the result stays deterministic and independent of U.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -113,6 +120,13 @@ __device__ __forceinline__ void load_b(const CUtensorMap* m, const GemmParams& p
     tma_load_2d_pair(dst, m, bar, nt * 128, row);
     tma_load_2d_pair(dst + 8192, m, bar, nt * 128 + 64, row);
   }
+}
+
+// Four fp32 additions into global memory, performed at L2.
+__device__ __forceinline__ void red_add_global_v4(float* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
 }
 
 template <int MN>
@@ -215,6 +229,7 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
     } else {  // GK_DWQKV
       frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
     }
+    const bool reduce = KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
       uint32_t v[32];
@@ -230,9 +245,15 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
                          pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
                          pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
         } else {
+          if (reduce) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              red_add_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_global_v4(frow + c4 * 32 + q * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
         }
       }
     }
@@ -259,7 +280,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // pairs share the A row block.
   const int m_pairs = (p.m_tiles + 1) / 2;
   const int n_pairs = (p.n_tiles + 1) / 2;
-  const int total = m_pairs * n_pairs;
+  const int tiles = m_pairs * n_pairs;
+  // Work unit t: pair tile t % tiles over K blocks [kb_lo(t), kb_hi(t)).
+  const bool ksplit = KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks;
+  const int total = ksplit ? 2 * tiles : tiles;
+  auto kb_lo = [&](int t) { return ksplit && t >= tiles ? p.k_mid : 0; };
+  auto kb_hi = [&](int t) { return ksplit && t < tiles ? p.k_mid : p.k_blocks; };
   const int t0 = blockIdx.x >> 1;
   const int G = gridDim.x >> 1;
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
@@ -302,11 +328,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int g = 0;  // k blocks issued so far, across tiles
       bool ok = true;
       for (int t = t0; ok && t < total; t += G) {
-        const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
+        const int tt = t % tiles;
+        const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
         const int mt_ld = mt < p.m_tiles ? mt : p.m_tiles - 1;  // a missing m tile reloads the last (unused)
-        const int ns = 2 * (t % n_pairs) + static_cast<int>(rank);
+        const int ns = 2 * (tt % n_pairs) + static_cast<int>(rank);
         const bool has_b = ns < p.n_tiles;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+        for (int kb = kb_lo(t); kb < kb_hi(t); ++kb, ++g) {
           const int s = g % kStages;
           // Polled: the arrival comes from the even CTA's commit, and a
           // suspended try_wait was measured to wake late for it.
@@ -341,7 +368,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t acc = tmem + b * 256;
         if (!(ok = mbar_spin<true>(bar(B_ACC_FREE + b), (i >> 1) & 1, w))) break;
         tc_fence_after();
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+        const int k0 = kb_lo(t);
+        for (int kb = k0; kb < kb_hi(t); ++kb, ++g) {
           const int s = g % kStages;
           if (!(ok = mbar_spin<true>(bar(B_FULL + s), (g / kStages) & 1, w))) break;
           tc_fence_after();
@@ -350,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             umma_bf16_pair(acc, operand_desc<Traits<KIND>::a_mn>(a, kk), operand_desc<Traits<KIND>::b_mn>(bb, kk),
-                           idesc, (carry_in || kb > 0 || kk > 0) ? 1u : 0u);
+                           idesc, (carry_in || kb > k0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (Lt::kSplit) {
 #pragma unroll
@@ -377,10 +405,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto prep = [&](int li, int t) {
       if constexpr (kCarry) {
         if (carry_in) {
-          const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
+          const int tt = t % tiles;
+          const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
           const int m = mt * 128 + r;
           const bool valid = mt < p.m_tiles && m < p.M;
-          const int nt0 = 2 * (t % n_pairs);
+          const int nt0 = 2 * (tt % n_pairs);
           const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
           for (int j = 0; j < nsl; ++j) {
             const float* crow = p.carry + static_cast<int64_t>(valid ? m : 0) * p.N + (nt0 + j) * 128;
@@ -411,8 +440,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int i = 0;
     for (int t = t0; ok && t < total; t += G, ++i) {
       const int b = i & 1;
-      const int mt = 2 * (t / n_pairs) + static_cast<int>(rank);
-      const int nt0 = 2 * (t % n_pairs);
+      const int tt = t % tiles;
+      const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
+      const int nt0 = 2 * (tt % n_pairs);
       const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
       const int m = mt * 128 + r;
       const bool tile_ok = mt < p.m_tiles;
@@ -480,7 +510,8 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
     if (e != cudaSuccess) return e;
     resident[dev] = n > 0 ? n : 1;
   }
-  const int total = ((p.m_tiles + 1) / 2) * ((p.n_tiles + 1) / 2);
+  const int tiles = ((p.m_tiles + 1) / 2) * ((p.n_tiles + 1) / 2);
+  const int total = (KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks) ? 2 * tiles : tiles;
   const int pairs = total < resident[dev] ? total : resident[dev];
   if (pairs <= 0) return cudaSuccess;
   gemm_kernel<KIND><<<2 * pairs, kThreads, smem, s>>>(a, b, p);

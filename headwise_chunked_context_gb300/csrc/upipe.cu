@@ -236,6 +236,48 @@ cudaError_t counted(int kind, cudaStream_t st, F&& launch) {
     if ((x) != cudaSuccess) return UPIPE_ERR_CUDA; \
   } while (0)
 #define UPIPE_LAUNCH(kind, x) UPIPE_CU(counted(kind, st, [&] { return (x); }))
+// dQ and dK/dV of one chunk run concurrently: neither reads what the other
+// writes.  dK/dV goes to a second stream of the device's greatest priority,
+// so its CTAs (few, long: key tile kb sees L - 128 kb queries of g_loc
+// heads) are dispatched first, and dQ's many short CTAs, heaviest first,
+// fill the SMs that the dK/dV tail leaves idle.  The stream and its fork /
+// join events are created on the first call per device.
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+Side g_side[kMaxDev];
+
+int side_stream(Side** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UPIPE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDev) return UPIPE_ERR_UNSUPPORTED_DEVICE;
+  Side& sd = g_side[dev];
+  if (!sd.join) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return UPIPE_ERR_CUDA;
+    if (!sd.s && cudaStreamCreateWithPriority(&sd.s, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return UPIPE_ERR_CUDA;
+    if (!sd.fork && cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
+  }
+  *out = &sd;
+  return UPIPE_OK;
+}
+
+int launch_attn_bwd_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const AttnBwdParams& b, int m_tiles, cudaStream_t st) {
+  Side* sd = nullptr;
+  if (int e = side_stream(&sd)) return e;
+  UPIPE_CU(cudaEventRecord(sd->fork, st));
+  UPIPE_CU(cudaStreamWaitEvent(sd->s, sd->fork, 0));
+  UPIPE_CU(counted(UPIPE_KIND_ATTN_BWD_DKDV, sd->s, [&] { return launch_attn_bwd_dkdv(mq, mk, mv, mdo, b, m_tiles, sd->s); }));
+  UPIPE_CU(counted(UPIPE_KIND_ATTN_BWD_DQ, st, [&] { return launch_attn_bwd_dq(mq, mk, mv, mdo, b, m_tiles, st); }));
+  UPIPE_CU(cudaEventRecord(sd->join, sd->s));
+  UPIPE_CU(cudaStreamWaitEvent(st, sd->join, 0));
+  return UPIPE_OK;
+}
+
 #define UPIPE_MAP(x)                                 \
   do {                                               \
     if (!(x)) return UPIPE_ERR_CUDA;                 \
@@ -529,8 +571,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     b.rope = rope;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st));
+    if (int e = launch_attn_bwd_pair(m_qkv, m_qkv, m_qkv, m_do, b, m_tiles, st)) return e;
 
     // dWqkv rows of the chunk: q slots always, k/v slots once complete.
     const int out_slots = emit_kv ? slots : s.U;
@@ -548,6 +589,11 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     wq.out = dWqkv;
     wq.ld_out = s.D;
     wq.lo_z = slots;
+    // K (tokens) in two halves reduced into zeroed rows; the split point
+    // depends on L alone.
+    wq.k_mid = wq.k_blocks >= 2 ? (wq.k_blocks + 1) / 2 : 0;
+    if (wq.k_mid > 0)
+      UPIPE_LAUNCH(UPIPE_KIND_ZERO_ROWS, launch_zero_rows(dWqkv, s.D, s.D, wq.tab1, out_slots, st));
     UPIPE_LAUNCH(UPIPE_KIND_DWQKV_GEMM, launch_gemm(GK_DWQKV, m_dqkv_mn, m_xmn, wq, st));
 
     // dx32 (+)= dqkv_c W_c, K slots in the canonical order: per KV group,
@@ -689,8 +735,7 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.rope = nullptr;
     b.status = status;
     b.limit_ns = limit;
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DQ, launch_attn_bwd_dq(mq, mk, mv, mdo, b, m_tiles, st));
-    UPIPE_LAUNCH(UPIPE_KIND_ATTN_BWD_DKDV, launch_attn_bwd_dkdv(mq, mk, mv, mdo, b, m_tiles, st));
+    if (int e = launch_attn_bwd_pair(mq, mk, mv, mdo, b, m_tiles, st)) return e;
   }
   return UPIPE_OK;
 }

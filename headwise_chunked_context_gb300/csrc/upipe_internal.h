@@ -19,8 +19,8 @@ constexpr int kMaxSlots = 96;     // H + 2 Hkv limit (per-slot tables below)
 
 // ------------------------------------------------------------------ GEMMs
 //
-// One tcgen05 GEMM kernel, 128x128 output tiles, K blocks of 64, serves the
-// six projection contractions of the layer.  The kind fixes which operands
+// One tcgen05 GEMM kernel (persistent CTA pairs, 256x256 output tiles, K
+// blocks of 64) serves the six projection contractions of the layer.  The kind fixes which operands
 // are K-major or MN-major, how tile coordinates map to tensor coordinates
 // and what the epilogue does.
 enum GemmKind : int {
@@ -52,6 +52,8 @@ struct GemmParams {
   const float* lse_in;         // DO: the chunk's LSE rows [U, L]
   float* ld_rec;               // DO: per 64-query tile records (see AttnBwdParams::ld)
   int lo_z;                    // DWQKV / DX: A slot offset of the low bf16 halves (0 = no split)
+  int k_mid;                   // DWQKV: > 0 splits K into blocks [0, k_mid) and [k_mid, k_blocks), two
+                               // work units per tile that add into the zeroed output (fp32 reductions)
   int* status;
   uint64_t limit_ns;
 };
@@ -116,6 +118,9 @@ cudaError_t launch_rope_table(float2* table, int64_t L, double theta, cudaStream
 cudaError_t launch_delta(const __nv_bfloat16* o, int64_t o_row, int64_t o_head, const __nv_bfloat16* dO,
                          int64_t do_row, int64_t do_head, const float* lse, float* ld, int64_t L, int nheads,
                          cudaStream_t s);
+// Zeroes the fp32 rows [128 b, 128 b + 128) x [0, cols) of `base` (leading
+// dimension ld) for the n row blocks b listed in `blocks`.
+cudaError_t launch_zero_rows(float* base, int64_t ld, int cols, const int16_t* blocks, int n, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace upipe

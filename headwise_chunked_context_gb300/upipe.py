@@ -44,7 +44,7 @@ EXPORTS = (
 )
 
 KINDS = ("rope_table", "qkv_gemm", "attn_fwd", "oproj_gemm", "do_gemm", "dwo_gemm", "attn_bwd_dq",
-         "attn_bwd_dkdv", "dwqkv_gemm", "dx_gemm", "delta")
+         "attn_bwd_dkdv", "dwqkv_gemm", "dx_gemm", "delta", "zero_rows")
 
 
 class UpipeError(RuntimeError):

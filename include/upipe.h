@@ -47,6 +47,14 @@
  *  - Work is enqueued on `stream` (a cudaStream_t, 0 = legacy default) and
  *    the call returns without waiting.  Calls that share a workspace must be
  *    ordered on the GPU (for example, issued on one stream).
+ *  - The backward entry points also enqueue on one library-owned stream per
+ *    device, created on the first backward call there with the device's
+ *    greatest stream priority: each chunk's dK/dV kernel runs on it, forked
+ *    from `stream` and joined back into it by events, while that chunk's dQ
+ *    kernel runs on `stream`.  All of a call's work is still ordered after
+ *    the work enqueued on `stream` before it, and work enqueued on `stream`
+ *    after it waits for all of it.  Make the first backward call on each
+ *    device outside stream capture.
  *
  * Errors
  * ------
@@ -166,11 +174,13 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
  *    GPU work (for example U = 1, Hkv = 1 fits up to about L = 32K tokens;
  *    U >= H/Hkv with U = 8 up to about L = 512K).
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and creates the
+ *    library's second stream and its events if no backward call has; make
+ *    that first call before any stream capture.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, no ordering) race.
- *  - Calls no cudaMalloc, cudaFree or allocating library routine.           */
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine, and after
+ *    the first call on a device creates no stream or event.                 */
 #define UPIPE_NOALLOC_SCRATCH_BYTES (32u << 20)
 int upipe_attn_core_bwd_noalloc(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq,
@@ -205,7 +215,8 @@ int upipe_debug_wait_timeout(uint64_t limit_ns, void* stream);
 #define UPIPE_KIND_DWQKV_GEMM 8
 #define UPIPE_KIND_DX_GEMM 9
 #define UPIPE_KIND_DELTA 10
-#define UPIPE_KIND_COUNT 11
+#define UPIPE_KIND_ZERO_ROWS 11
+#define UPIPE_KIND_COUNT 12
 int64_t upipe_launch_count(void);
 void upipe_profile_enable(int on);
 int upipe_profile_read(double* ms, int64_t* launches, int n);
