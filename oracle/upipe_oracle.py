@@ -26,7 +26,7 @@ oracle is the plain definition of one GQA/RoPE attention layer:
 * backward: the exact gradient of ``sum(out * dout)`` via the closed-form
   softmax backward.
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
 
 * RoPE pairs (i, i + d/2) ("rotate-half"), angle p * theta^(-2i/d) in fp64,
   rotation by +angle; no frequency scaling.

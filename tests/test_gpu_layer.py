@@ -52,7 +52,10 @@ def test_tiny_config_matches_oracle():
     _check_vs_oracle(synth.TINY, inputs, outs)
 
 
-@pytest.mark.parametrize("L,D,H,Hkv,U", [(200, 256, 4, 2, 2), (129, 128, 4, 1, 1), (384, 384, 8, 2, 4)])
+# L = 1 and 64: one K block in the weight-gradient GEMM (no K split); 65: two
+# blocks, the second holding one token.
+@pytest.mark.parametrize("L,D,H,Hkv,U", [(200, 256, 4, 2, 2), (129, 128, 4, 1, 1), (384, 384, 8, 2, 4),
+                                         (1, 128, 2, 1, 1), (64, 256, 4, 2, 2), (65, 256, 4, 2, 2)])
 def test_ragged_layers_match_oracle(L, D, H, Hkv, U):
     shape = synth.LayerShape(L=L, D=D, H=H, Hkv=Hkv, U=U)
     inputs, outs = _run(shape, U)
