@@ -429,7 +429,8 @@ def run_upipe(args, w, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, **w, "d": 128, "rope_theta": 500000.0, "causal": True,
                    "o_saved": False, "flops_per_step": step_flops, "attn_flops_per_step": attn_f,
-                   "l2": "inputs larger than L2 (x, dout 256 MiB each at L=32768)",
+                   "l2": (f"inputs larger than L2 (x, dout {L * D * 2 / 2**20:.0f} MiB each)" if 2 * L * D * 2 > 129e6
+                          else f"inputs fit in L2 (x, dout {L * D * 2 / 2**20:.1f} MiB each; not flushed)"),
                    "parallelism": f"replicas x{world}"},
         "pct_bf16_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
                           "peaks": f"{burst}/{sustained} TFLOP/s ({peak_src})"},
