@@ -57,7 +57,12 @@ struct Layout {
   static constexpr int kA = kSplit ? 2 * kTile : kTile;
   static constexpr int kB = kTile;  // this CTA's 128-column slot of the pair's 256
   static constexpr int kStage = kA + kB;
-  static constexpr int OFF_BAR = kStages * kStage;
+  // Carry kinds: a 32 x 32 fp32 staging tile per epilogue warp (4 KB), through
+  // which the carry rows are transposed so that global accesses are whole
+  // 128-byte lines.
+  static constexpr bool kCarryKind = (KIND == GK_OPROJ || KIND == GK_DX);
+  static constexpr int OFF_XPOSE = kStages * kStage;
+  static constexpr int OFF_BAR = OFF_XPOSE + (kCarryKind ? 4 * 4096 : 0);
   static constexpr int B_FULL = 0;                    // even CTA: both CTAs' copies of the stage landed
   static constexpr int B_EMPTY = kStages;             // the pair's products read the stage
   static constexpr int B_ACC_FULL = 2 * kStages;      // per accumulator: products done
@@ -135,11 +140,63 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
   else return sdesc_sw128(base + kk * 32, 16, 1024);
 }
 
+// Staging-tile address of 16-byte chunk `chunk` of row `row`: rows of 128 B,
+// chunks XOR-swizzled by row & 7, so that a warp writing one row per lane and
+// a warp reading four rows of eight lanes each both touch every bank once
+// per 128 bytes.
+__device__ __forceinline__ uint32_t xpose_addr(uint32_t base, int row, int chunk) {
+  return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// Carry rows m0 .. m0 + 31 (one per lane), columns col .. col + 31, between
+// the fp32 carry in global memory and registers, through the warp's staging
+// tile `xs`: global accesses go four rows of 128 B per instruction instead of
+// 32 rows of 16 B.  All 32 lanes call these together.
+__device__ __forceinline__ void carry_store32(const GemmParams& p, uint32_t xs, int m0, int col,
+                                              const uint32_t (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) st_shared_v4(xpose_addr(xs, lane, q), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = 4 * i + (lane >> 3);
+    const uint4 y = ld_shared_v4(xpose_addr(xs, row, lane & 7));
+    if (m0 + row < p.M)
+      st_global_v4(p.carry + static_cast<int64_t>(m0 + row) * p.N + col + (lane & 7) * 4, y.x, y.y, y.z, y.w);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void carry_load32(const GemmParams& p, uint32_t xs, int m0, int col, bool tile_ok,
+                                             uint32_t (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = 4 * i + (lane >> 3);
+    const uint4 y = tile_ok && m0 + row < p.M
+                        ? ld_global_nc_v4(p.carry + static_cast<int64_t>(m0 + row) * p.N + col + (lane & 7) * 4)
+                        : make_uint4(0, 0, 0, 0);
+    st_shared_v4(xpose_addr(xs, row, lane & 7), y.x, y.y, y.z, y.w);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 y = ld_shared_v4(xpose_addr(xs, lane, q));
+    v[4 * q] = y.x;
+    v[4 * q + 1] = y.y;
+    v[4 * q + 2] = y.z;
+    v[4 * q + 3] = y.w;
+  }
+  __syncwarp();
+}
+
 // Writes one 128-column slot of a finished accumulator (TMEM row address
-// `trow`, one output row per thread) in the kind's output format.
+// `trow`, one output row per thread) in the kind's output format; `xs` is
+// the warp's staging tile (carry kinds).
 template <int KIND>
 __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, int m, int r, int mt, int nt,
-                                           bool valid) {
+                                           bool valid, uint32_t xs) {
   constexpr bool kCarry = (KIND == GK_OPROJ || KIND == GK_DX);
   if constexpr (KIND == GK_QKV) {
     const int slot = nt;
@@ -230,6 +287,19 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
       frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
     }
     const bool reduce = KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks;
+    if constexpr (kCarry) {
+      if (!p.final_out) {
+        const int m0 = m - (r & 31);
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(trow + c4 * 32, v);
+          tmem_ld_wait(v);
+          carry_store32(p, xs, m0, nt * 128 + c4 * 32, v);
+        }
+        return;
+      }
+    }
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
       uint32_t v[32];
@@ -399,6 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t trow0 = tmem_lane_addr(tmem, quad, 0);
+    const uint32_t xs = sb + Lt::OFF_XPOSE + quad * 4096;  // carry kinds only
     const uint32_t acc_free_even = mapa_shared(bar(B_ACC_FREE), 0);
     // Makes accumulator (local tile li) & 1 ready for pair tile t: loads this
     // CTA's rows of the carry when there is one, then tells the even CTA.
@@ -407,23 +478,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (carry_in) {
           const int tt = t % tiles;
           const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
-          const int m = mt * 128 + r;
-          const bool valid = mt < p.m_tiles && m < p.M;
+          const int m0 = mt * 128 + quad * 32;  // row of lane 0
           const int nt0 = 2 * (tt % n_pairs);
           const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
           for (int j = 0; j < nsl; ++j) {
-            const float* crow = p.carry + static_cast<int64_t>(valid ? m : 0) * p.N + (nt0 + j) * 128;
-#pragma unroll
+#pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
               uint32_t v[32];
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                uint4 x = valid ? ld_global_nc_v4(crow + c4 * 32 + q * 4) : make_uint4(0, 0, 0, 0);
-                v[4 * q] = x.x;
-                v[4 * q + 1] = x.y;
-                v[4 * q + 2] = x.z;
-                v[4 * q + 3] = x.w;
-              }
+              carry_load32(p, xs, m0, (nt0 + j) * 128 + c4 * 32, mt < p.m_tiles, v);
               tmem_st32(trow0 + (li & 1) * 256 + j * 128 + c4 * 32, v);
             }
           }
@@ -452,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (tile_ok) {
         for (int j = 0; j < nsl; ++j) {
           const uint32_t trow = trow0 + b * 256 + j * 128;
-          store_slot<KIND>(p, trow, m, r, mt, nt0 + j, valid);
+          store_slot<KIND>(p, trow, m, r, mt, nt0 + j, valid, xs);
         }
       }
       if (t + 2 * G < total) prep(i + 2, t + 2 * G);
