@@ -53,16 +53,19 @@ constexpr int kTile = 128 * 64 * 2;  // one 16 KB operand tile (128 x 64 bf16)
 template <int KIND>
 struct Layout {
   static constexpr bool kSplit = (KIND == GK_DWQKV || KIND == GK_DX);
-  static constexpr int kStages = kSplit ? 4 : 6;
+  static constexpr int kStages = kSplit ? 4 : (KIND == GK_OPROJ ? 5 : 6);
   static constexpr int kA = kSplit ? 2 * kTile : kTile;
   static constexpr int kB = kTile;  // this CTA's 128-column slot of the pair's 256
   static constexpr int kStage = kA + kB;
-  // Carry kinds: a 32 x 32 fp32 staging tile per epilogue warp (4 KB), through
-  // which the carry rows are transposed so that global accesses are whole
-  // 128-byte lines.
+  // Carry kinds: kXposeChunks 32 x 32 fp32 staging tiles per epilogue warp
+  // (4 KB each), through which the carry rows are transposed so that global
+  // accesses are whole 128-byte lines.  The O projection (K = U d, short
+  // products) stages a whole 128-column slot so that its carry loads are in
+  // flight together; dx hides one chunk at a time behind its longer products.
   static constexpr bool kCarryKind = (KIND == GK_OPROJ || KIND == GK_DX);
+  static constexpr int kXposeChunks = KIND == GK_OPROJ ? 4 : 1;
   static constexpr int OFF_XPOSE = kStages * kStage;
-  static constexpr int OFF_BAR = OFF_XPOSE + (kCarryKind ? 4 * 4096 : 0);
+  static constexpr int OFF_BAR = OFF_XPOSE + (kCarryKind ? 4 * kXposeChunks * 4096 : 0);
   static constexpr int B_FULL = 0;                    // even CTA: both CTAs' copies of the stage landed
   static constexpr int B_EMPTY = kStages;             // the pair's products read the stage
   static constexpr int B_ACC_FULL = 2 * kStages;      // per accumulator: products done
@@ -168,18 +171,28 @@ __device__ __forceinline__ void carry_store32(const GemmParams& p, uint32_t xs, 
   __syncwarp();
 }
 
-__device__ __forceinline__ void carry_load32(const GemmParams& p, uint32_t xs, int m0, int col, bool tile_ok,
-                                             uint32_t (&v)[32]) {
+// Starts the copy of carry columns col .. col + 31 of rows m0 .. m0 + 31 into
+// staging tile `xs` (asynchronous 16-byte copies, four rows of 128 B per
+// warp instruction; rows past M or a missing tile are zero-filled).
+__device__ __forceinline__ void carry_fetch32(const GemmParams& p, uint32_t xs, int m0, int col, bool tile_ok) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int row = 4 * i + (lane >> 3);
-    const uint4 y = tile_ok && m0 + row < p.M
-                        ? ld_global_nc_v4(p.carry + static_cast<int64_t>(m0 + row) * p.N + col + (lane & 7) * 4)
-                        : make_uint4(0, 0, 0, 0);
-    st_shared_v4(xpose_addr(xs, row, lane & 7), y.x, y.y, y.z, y.w);
+    const uint32_t dst = xpose_addr(xs, row, lane & 7);
+    if (tile_ok && m0 + row < p.M) {
+      const float* src = p.carry + static_cast<int64_t>(m0 + row) * p.N + col + (lane & 7) * 4;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    } else {
+      st_shared_v4(dst, 0u, 0u, 0u, 0u);
+    }
   }
-  __syncwarp();
+}
+
+// After the fetches and a cp.async.wait_all + __syncwarp: lane's row of
+// staging tile `xs`.
+__device__ __forceinline__ void carry_row32(uint32_t xs, uint32_t (&v)[32]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const uint4 y = ld_shared_v4(xpose_addr(xs, lane, q));
@@ -188,7 +201,6 @@ __device__ __forceinline__ void carry_load32(const GemmParams& p, uint32_t xs, i
     v[4 * q + 2] = y.z;
     v[4 * q + 3] = y.w;
   }
-  __syncwarp();
 }
 
 // Writes one 128-column slot of a finished accumulator (TMEM row address
@@ -469,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t trow0 = tmem_lane_addr(tmem, quad, 0);
-    const uint32_t xs = sb + Lt::OFF_XPOSE + quad * 4096;  // carry kinds only
+    const uint32_t xs = sb + Lt::OFF_XPOSE + quad * Lt::kXposeChunks * 4096;  // carry kinds only
     const uint32_t acc_free_even = mapa_shared(bar(B_ACC_FREE), 0);
     // Makes accumulator (local tile li) & 1 ready for pair tile t: loads this
     // CTA's rows of the carry when there is one, then tells the even CTA.
@@ -481,12 +493,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int m0 = mt * 128 + quad * 32;  // row of lane 0
           const int nt0 = 2 * (tt % n_pairs);
           const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
+          constexpr int kXC = Lt::kXposeChunks;
           for (int j = 0; j < nsl; ++j) {
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-              uint32_t v[32];
-              carry_load32(p, xs, m0, (nt0 + j) * 128 + c4 * 32, mt < p.m_tiles, v);
-              tmem_st32(trow0 + (li & 1) * 256 + j * 128 + c4 * 32, v);
+            for (int c0 = 0; c0 < 4; c0 += kXC) {
+#pragma unroll
+              for (int c = 0; c < kXC; ++c)
+                carry_fetch32(p, xs + c * 4096, m0, (nt0 + j) * 128 + (c0 + c) * 32, mt < p.m_tiles);
+              asm volatile("cp.async.wait_all;" ::: "memory");
+              __syncwarp();
+#pragma unroll 1
+              for (int c = 0; c < kXC; ++c) {
+                uint32_t v[32];
+                carry_row32(xs + c * 4096, v);
+                tmem_st32(trow0 + (li & 1) * 256 + j * 128 + (c0 + c) * 32, v);
+              }
+              __syncwarp();
             }
           }
           tmem_st_wait();
