@@ -32,6 +32,19 @@ def test_header_declares_what_binding_uses():
     assert declared_symbols() == sorted(upipe.EXPORTS)
 
 
+def test_kernel_kinds_match_the_header():
+    """upipe.KINDS names the UPIPE_KIND_* values in order, and its length is
+    UPIPE_KIND_COUNT, so profile_read() labels every kind correctly."""
+    text = open(HEADER).read()
+    kinds = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define UPIPE_KIND_([A-Z0-9_]+) (\d+)", text)}
+    count = kinds.pop("COUNT")
+    assert count == len(upipe.KINDS)
+    assert sorted(kinds.values()) == list(range(count))
+    for name, value in kinds.items():
+        words = set(name.lower().split("_"))
+        assert words <= set(upipe.KINDS[value].split("_")) | {"attn", "gemm", "bwd", "fwd"}, (name, upipe.KINDS[value])
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
