@@ -33,12 +33,19 @@
 // loaded into TMEM before the first MMA so that chunked and unchunked runs
 // perform the same fp32 additions in the same order.
 //
-// dWqkv (K = L tokens, only (U + 2 Hkv_c) / 2 x D / 256 pair tiles: 96 for
-// the 8B layer at U = 8, 1.26 waves of 76 pairs) splits K at k_mid into two
-// work units per tile, each reduced (red.global.add.f32) into the zeroed
-// output: 192 units fill the pairs 2.5 times instead of 1.26.  Two addends
-// into a zero give the same bits in either order, and k_mid depends only on
-// L, so the result stays deterministic and independent of U.
+// dWqkv has K = L tokens but only ((U + 2 Hkv_c) / 2) x (D / 256) pair
+// tiles (96 for D = 4096, U = 8 query and 2 KV heads: 1.26 waves of 76
+// pairs), so it splits K at k_mid into two work units per tile, each reduced
+// (red.global.add.f32) into the zeroed output: 192 units fill the pairs 2.5
+// times instead of 1.26.  Two addends into a zero give the same bits in
+// either order, and k_mid depends only on L, so the result stays
+// deterministic and independent of U.
+//
+// The carried fp32 partials (out32, dx32) move between global memory and the
+// epilogue warps through a swizzled shared staging tile per warp: TMEM gives
+// each lane one row, and 16-byte accesses to 32 different rows per warp
+// instruction left the carry stream latency-bound; through the tile, each
+// global access instruction covers four whole 128-byte rows.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
