@@ -444,7 +444,6 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
   const int64_t L = s.L;
   const int slots = s.U + 2 * s.kvc;
   const int m_tiles = static_cast<int>((L + 127) / 128);
-  const int q64_tiles = static_cast<int>((L + 63) / 64);
   const int64_t Hd = static_cast<int64_t>(s.H) * 128;
   const float scale = static_cast<float>(1.0 / std::sqrt(128.0));
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
