@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -247,6 +248,10 @@ struct Side {
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 Side g_side[kMaxDev];
+// Serialises the fork / launch / join sequence: the fork and join events are
+// shared, and a stream wait takes the event as last recorded, so two host
+// threads interleaving their sequences could join the wrong work.
+std::mutex g_side_mu;
 
 int side_stream(Side** out) {
   int dev = 0;
@@ -267,6 +272,7 @@ int side_stream(Side** out) {
 
 int launch_attn_bwd_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const AttnBwdParams& b, int m_tiles, cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_side_mu);
   Side* sd = nullptr;
   if (int e = side_stream(&sd)) return e;
   UPIPE_CU(cudaEventRecord(sd->fork, st));

@@ -55,6 +55,9 @@
  *    the work enqueued on `stream` before it, and work enqueued on `stream`
  *    after it waits for all of it.  Make the first backward call on each
  *    device outside stream capture.
+ *  - Entry points may be called from several host threads (calls that share
+ *    a workspace still need GPU ordering); the launch counter and the
+ *    profiling hooks below are meant for one thread.
  *
  * Errors
  * ------
