@@ -6,6 +6,9 @@
 // chunk holds fewer query heads than a KV group, the fp32 dK/dV carry) lives
 // in a fixed array in this module's static device memory instead of a
 // caller-supplied workspace.
+#include <atomic>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "upipe.h"
@@ -18,7 +21,8 @@ namespace {
 __device__ __align__(256) unsigned char g_upipe_noalloc_scratch[UPIPE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDev = 64;
-void* g_scratch_addr[kMaxDev];  // device address of the array, per device
+std::atomic<void*> g_scratch_addr[kMaxDev];  // device address of the array, per device
+std::mutex g_scratch_mu;
 
 }  // namespace
 
@@ -37,16 +41,22 @@ extern "C" int upipe_attn_core_bwd_noalloc(const upipe_cfg* cfg, const uint16_t*
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return UPIPE_ERR_CUDA;
   if (major != 10 || minor != 3) return UPIPE_ERR_UNSUPPORTED_DEVICE;
-  if (!g_scratch_addr[dev]) {
+  void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!scratch) {
     // Once per device, with that device current: the array's name is only a
     // host-side stand-in; kernels need its device address.
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_upipe_noalloc_scratch) != cudaSuccess || addr == nullptr)
-      return UPIPE_ERR_CUDA;
-    g_scratch_addr[dev] = addr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    scratch = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!scratch) {
+      if (cudaGetSymbolAddress(&scratch, g_upipe_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+        return UPIPE_ERR_CUDA;
+      g_scratch_addr[dev].store(scratch, std::memory_order_release);
+    }
   }
   // Nothing in the scratch has to start at zero: every record and carry is
-  // written before it is read within one call.
-  return upipe_attn_core_bwd(cfg, q, k, v, o, lse, dout_o, dq, dk, dv, g_scratch_addr[dev],
-                             UPIPE_NOALLOC_SCRATCH_BYTES, stream);
+  // written before it is read within one call.  Profiling events are not
+  // recorded for this call's launches (recording may create events).
+  upipe::ProfilingOff no_events;
+  return upipe_attn_core_bwd(cfg, q, k, v, o, lse, dout_o, dq, dk, dv, scratch, UPIPE_NOALLOC_SCRATCH_BYTES,
+                             stream);
 }

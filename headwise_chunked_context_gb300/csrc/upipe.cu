@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <initializer_list>
 #include <mutex>
 #include <vector>
@@ -128,46 +129,54 @@ uint64_t spin_limit_ns() {
   return 2000000000ull;
 }
 
-// Device checks and the status word address, cached per device.
+// Device checks and the status word address, cached per device.  The first
+// call on a device fills its entry under a lock; later calls read it through
+// an acquire load, so calls from several host threads see a complete entry.
 constexpr int kMaxDev = 64;
-int g_dev_state[kMaxDev];  // 0 unknown, 1 ok, -1 unsupported
+std::atomic<int> g_dev_state[kMaxDev];  // 0 unknown, 1 ok, -1 unsupported
 int* g_status_ptr[kMaxDev];
+std::mutex g_dev_mu;
 
 int device_ready(int** status) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return UPIPE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDev) return UPIPE_ERR_UNSUPPORTED_DEVICE;
-  if (g_dev_state[dev] == 0) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return UPIPE_ERR_CUDA;
-    if (major != 10 || minor != 3) {
-      g_dev_state[dev] = -1;
-    } else {
-      void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_upipe_status) != cudaSuccess) return UPIPE_ERR_CUDA;
-      g_status_ptr[dev] = static_cast<int*>(ptr);
-      g_dev_state[dev] = 1;
+  if (g_dev_state[dev].load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_dev_state[dev].load(std::memory_order_relaxed) == 0) {
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return UPIPE_ERR_CUDA;
+      if (major != 10 || minor != 3) {
+        g_dev_state[dev].store(-1, std::memory_order_release);
+      } else {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_upipe_status) != cudaSuccess) return UPIPE_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int*>(ptr);
+        g_dev_state[dev].store(1, std::memory_order_release);
+      }
     }
   }
-  if (g_dev_state[dev] < 0) return UPIPE_ERR_UNSUPPORTED_DEVICE;
+  if (g_dev_state[dev].load(std::memory_order_acquire) < 0) return UPIPE_ERR_UNSUPPORTED_DEVICE;
   *status = g_status_ptr[dev];
   return UPIPE_OK;
 }
 
 // ------------------------------------------------------------ tensor maps
 
+// Looked up once (a function-local static is initialised exactly once, even
+// when several threads arrive together).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -199,9 +208,12 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t heads, uint
 }
 
 // Launch accounting: a counter of every kernel launch, and optional CUDA
-// event pairs recorded around each launch on the launching stream.
-int64_t g_launches = 0;
-bool g_profile = false;
+// event pairs recorded around each launch on the launching stream.  A host
+// thread inside the entry point that allocates nothing records no events
+// (an event pair may need cudaEventCreate and grows a host vector).
+std::atomic<int64_t> g_launches{0};
+std::atomic<bool> g_profile{false};
+thread_local bool t_no_profile = false;
 struct ProfRec {
   int kind;
   cudaEvent_t a, b;
@@ -220,10 +232,18 @@ cudaEvent_t pool_event() {
   return e;
 }
 
+}  // namespace
+
+// See upipe_internal.h.
+ProfilingOff::ProfilingOff() : prev_(t_no_profile) { t_no_profile = true; }
+ProfilingOff::~ProfilingOff() { t_no_profile = prev_; }
+
+namespace {
+
 template <class F>
 cudaError_t counted(int kind, cudaStream_t st, F&& launch) {
-  ++g_launches;
-  if (!g_profile) return launch();
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_profile.load(std::memory_order_relaxed) || t_no_profile) return launch();
   ProfRec r{kind, pool_event(), pool_event()};
   cudaEventRecord(r.a, st);
   const cudaError_t e = launch();
@@ -333,6 +353,26 @@ int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int ha
   if (chunk_bytes) *chunk_bytes = p.chunk_bytes();
   if (fixed_bytes) *fixed_bytes = p.fixed_bytes();
   return UPIPE_OK;
+}
+
+int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int has_o_saved) {
+  if (!cfg || pass < 0 || pass > 2) return UPIPE_ERR_INVALID_ARG;
+  upipe_cfg c = *cfg;
+  Shape s;
+  c.U = c.H;  // U = H is valid whenever the rest of the configuration is
+  if (!check_cfg(&c, !core_only, &s)) return UPIPE_ERR_INVALID_ARG;
+  for (int u = c.H; u >= 1; --u) {
+    c.U = u;
+    if (!check_cfg(&c, !core_only, &s)) continue;
+    size_t need = 0;
+    for (int ps = 0; ps < 2; ++ps)
+      if (pass == 2 || pass == ps) {
+        const size_t b = make_plan(s, ps, core_only != 0, has_o_saved != 0).total;
+        need = b > need ? b : need;
+      }
+    if (need <= budget_bytes) return u;
+  }
+  return UPIPE_ERR_WS_TOO_SMALL;
 }
 
 int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo, uint16_t* out,
@@ -763,9 +803,9 @@ int upipe_debug_wait_timeout(uint64_t limit_ns, void* stream) {
                                                                                                    : UPIPE_ERR_CUDA;
 }
 
-int64_t upipe_launch_count(void) { return g_launches; }
+int64_t upipe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-void upipe_profile_enable(int on) { g_profile = on != 0; }
+void upipe_profile_enable(int on) { g_profile.store(on != 0, std::memory_order_relaxed); }
 
 int upipe_profile_read(double* ms, int64_t* launches, int n) {
   for (int k = 0; k < n; ++k) {

@@ -102,6 +102,20 @@ struct AttnBwdParams {
   uint64_t limit_ns;
 };
 
+// While an object of this type lives, launches made by the current host
+// thread record no profiling events (the entry point that allocates nothing
+// must not create events or grow host vectors).
+class ProfilingOff {
+ public:
+  ProfilingOff();
+  ~ProfilingOff();
+  ProfilingOff(const ProfilingOff&) = delete;
+  ProfilingOff& operator=(const ProfilingOff&) = delete;
+
+ private:
+  bool prev_;
+};
+
 // ------------------------------------------------------------- launchers
 
 cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,

@@ -30,6 +30,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 EXPORTS = (
     "upipe_workspace_bytes",
     "upipe_activation_bytes",
+    "upipe_choose_u",
     "upipe_attn_fwd",
     "upipe_attn_bwd",
     "upipe_attn_core_fwd",
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.upipe_activation_bytes.restype = ctypes.c_int
         L.upipe_activation_bytes.argtypes = [cfgp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+        L.upipe_choose_u.restype = ctypes.c_int
+        L.upipe_choose_u.argtypes = [cfgp, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.upipe_attn_fwd.restype = ctypes.c_int
         L.upipe_attn_fwd.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_bwd.restype = ctypes.c_int
@@ -153,8 +156,35 @@ def _stream(stream=None):
 
 
 def _expect(t, shape, dtype, name):
+    """Checks one tensor argument's shape and dtype before anything reaches
+    the library: the kernels read and write exactly the sizes the
+    configuration implies, so a smaller tensor must be refused here."""
+    if t is None:
+        raise ValueError(f"{name}: missing")
     if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
         raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+
+
+def _on_device(**tensors):
+    """Every tensor argument must be a contiguous CUDA tensor on the current
+    device (the kernels run there and take raw pointers)."""
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name}: expected a CUDA tensor, got one on {t.device}")
+        if t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+def _expect_ws(ws, need, name="ws"):
+    if ws is None:
+        return
+    _on_device(**{name: ws})
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"{name}: {ws.numel() * ws.element_size()} bytes, the call needs {need}")
 
 
 # ----------------------------------------------------------- raw entry points
@@ -173,22 +203,57 @@ def activation_bytes(cfg: Config, pass_: int, core_only: bool = False, has_o_sav
     return int(chunk.value), int(fixed.value)
 
 
+def choose_u(cfg: Config, budget_bytes: int, pass_: int = 2, core_only: bool = False,
+             has_o_saved: bool = False) -> int:
+    """Largest valid chunk size U whose workspace fits `budget_bytes`
+    (upipe_choose_u; cfg.U is ignored).  pass_ 0 = forward, 1 = backward,
+    2 = the larger of the two.  Raises UpipeError when no U fits."""
+    c = cfg.c()
+    r = int(lib().upipe_choose_u(ctypes.byref(c), int(budget_bytes), pass_, int(core_only), int(has_o_saved)))
+    if r < 0:
+        raise UpipeError(r, "upipe_choose_u")
+    return r
+
+
 def _ws(cfg, pass_, core_only, has_o_saved, ws, device):
     need = workspace_bytes(cfg, pass_, core_only, has_o_saved)
     if ws is None:
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    _expect_ws(ws, need)
     return ws, ws.numel() * ws.element_size()
 
 
-def attn_fwd(cfg: Config, x, Wqkv, Wo, out, lse, o_saved=None, ws=None, stream=None):
+def _layer_tensors(cfg: Config, x, Wqkv, Wo, lse, o_saved):
     L, D, H, Hkv = cfg.L, cfg.D, cfg.H, cfg.Hkv
     _expect(x, (L, D), torch.bfloat16, "x")
     _expect(Wqkv, ((H + 2 * Hkv) * 128, D), torch.bfloat16, "Wqkv")
     _expect(Wo, (D, H * 128), torch.bfloat16, "Wo")
-    _expect(out, (L, D), torch.bfloat16, "out")
     _expect(lse, (H, L), torch.float32, "lse")
     if o_saved is not None:
         _expect(o_saved, (L, H * 128), torch.bfloat16, "o_saved")
+
+
+def _core_tensors(cfg: Config, q, k, v, lse, o=None):
+    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
+    _expect(q, (L, H, 128), torch.bfloat16, "q")
+    _expect(k, (L, Hkv, 128), torch.bfloat16, "k")
+    _expect(v, (L, Hkv, 128), torch.bfloat16, "v")
+    _expect(lse, (H, L), torch.float32, "lse")
+    if o is not None:
+        _expect(o, (L, H, 128), torch.bfloat16, "o")
+
+
+def _core_grads(cfg: Config, do, dq, dk, dv):
+    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
+    for t, shp, n in ((do, (L, H, 128), "dout_o"), (dq, (L, H, 128), "dq"), (dk, (L, Hkv, 128), "dk"),
+                      (dv, (L, Hkv, 128), "dv")):
+        _expect(t, shp, torch.bfloat16, n)
+
+
+def attn_fwd(cfg: Config, x, Wqkv, Wo, out, lse, o_saved=None, ws=None, stream=None):
+    _layer_tensors(cfg, x, Wqkv, Wo, lse, o_saved)
+    _expect(out, (cfg.L, cfg.D), torch.bfloat16, "out")
+    _on_device(x=x, Wqkv=Wqkv, Wo=Wo, out=out, lse=lse, o_saved=o_saved)
     ws, nbytes = _ws(cfg, 0, False, o_saved is not None, ws, x.device)
     c = cfg.c()
     _check(lib().upipe_attn_fwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(out), _ptr(lse),
@@ -197,11 +262,12 @@ def attn_fwd(cfg: Config, x, Wqkv, Wo, out, lse, o_saved=None, ws=None, stream=N
 
 def attn_bwd(cfg: Config, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved=None, ws=None, stream=None):
     L, D, H, Hkv = cfg.L, cfg.D, cfg.H, cfg.Hkv
+    _layer_tensors(cfg, x, Wqkv, Wo, lse, o_saved)
     _expect(dout, (L, D), torch.bfloat16, "dout")
     _expect(dx, (L, D), torch.bfloat16, "dx")
     _expect(dWqkv, ((H + 2 * Hkv) * 128, D), torch.float32, "dWqkv")
     _expect(dWo, (D, H * 128), torch.float32, "dWo")
-    _expect(lse, (H, L), torch.float32, "lse")
+    _on_device(x=x, Wqkv=Wqkv, Wo=Wo, dout=dout, lse=lse, o_saved=o_saved, dx=dx, dWqkv=dWqkv, dWo=dWo)
     ws, nbytes = _ws(cfg, 1, False, o_saved is not None, ws, x.device)
     c = cfg.c()
     _check(lib().upipe_attn_bwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(dout), _ptr(lse),
@@ -210,26 +276,22 @@ def attn_bwd(cfg: Config, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved=None, 
 
 
 def attn_core_fwd(cfg: Config, q, k, v, o, lse, ws=None, stream=None):
-    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
-    _expect(q, (L, H, 128), torch.bfloat16, "q")
-    _expect(k, (L, Hkv, 128), torch.bfloat16, "k")
-    _expect(v, (L, Hkv, 128), torch.bfloat16, "v")
-    _expect(o, (L, H, 128), torch.bfloat16, "o")
-    _expect(lse, (H, L), torch.float32, "lse")
+    _core_tensors(cfg, q, k, v, lse, o)
+    _on_device(q=q, k=k, v=v, o=o, lse=lse)
     need = workspace_bytes(cfg, 0, True)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     if need and ws is None:
         ws, nbytes = _ws(cfg, 0, True, False, None, q.device)
+    _expect_ws(ws, need)
     c = cfg.c()
     _check(lib().upipe_attn_core_fwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                      _ptr(ws), nbytes, _stream(stream)), "upipe_attn_core_fwd")
 
 
 def attn_core_bwd(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, ws=None, stream=None):
-    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
-    for t, shp, n in ((do, (L, H, 128), "dout_o"), (dq, (L, H, 128), "dq"), (dk, (L, Hkv, 128), "dk"),
-                      (dv, (L, Hkv, 128), "dv")):
-        _expect(t, shp, torch.bfloat16, n)
+    _core_tensors(cfg, q, k, v, lse, o)
+    _core_grads(cfg, do, dq, dk, dv)
+    _on_device(q=q, k=k, v=v, o=o, lse=lse, dout_o=do, dq=dq, dk=dk, dv=dv)
     ws, nbytes = _ws(cfg, 1, True, False, ws, q.device)
     c = cfg.c()
     _check(lib().upipe_attn_core_bwd(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
@@ -241,10 +303,9 @@ def attn_core_bwd_noalloc(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, stream=N
     """Core backward through the entry point that allocates nothing (its
     scratch is a fixed array in the library's static device memory; see
     include/upipe.h).  For callers that may not allocate at call time."""
-    L, H, Hkv = cfg.L, cfg.H, cfg.Hkv
-    for t, shp, n in ((do, (L, H, 128), "dout_o"), (dq, (L, H, 128), "dq"), (dk, (L, Hkv, 128), "dk"),
-                      (dv, (L, Hkv, 128), "dv")):
-        _expect(t, shp, torch.bfloat16, n)
+    _core_tensors(cfg, q, k, v, lse, o)
+    _core_grads(cfg, do, dq, dk, dv)
+    _on_device(q=q, k=k, v=v, o=o, lse=lse, dout_o=do, dq=dq, dk=dk, dv=dv)
     c = cfg.c()
     _check(lib().upipe_attn_core_bwd_noalloc(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                              _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),

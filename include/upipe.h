@@ -124,6 +124,22 @@ size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int 
 int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved,
                            size_t* chunk_bytes, size_t* fixed_bytes);
 
+/* Largest chunk size U whose workspace fits a memory budget.  The talk
+ * write-up's chunk-size ablation paragraph: larger chunks compute more heads
+ * at once, use more memory and run somewhat faster, so a run picks the
+ * headwise chunk size that fits its memory budget.
+ *   cfg          every field but U is read (U is ignored)
+ *   budget_bytes bytes the caller can give the workspace
+ *   pass         0 = forward workspace, 1 = backward, 2 = the larger of the
+ *                two (one workspace serving a whole training step)
+ *   core_only, has_o_saved as for upipe_workspace_bytes
+ * Considers every valid U (H % U == 0, and U % g == 0 or g % U == 0) and
+ * returns the largest whose workspace is <= budget_bytes (the workspace is
+ * not monotone in U: U = H drops the fp32 output carry).  Returns
+ * UPIPE_ERR_INVALID_ARG for an invalid configuration or pass, and
+ * UPIPE_ERR_WS_TOO_SMALL when no valid U fits.  Host arithmetic only.      */
+int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int has_o_saved);
+
 /* Layer forward (the write-up's paragraph on intermediate buffers).
  *   x        [L, D] bf16                 Wqkv [(H+2Hkv)*128, D] bf16
  *   Wo       [D, H*128] bf16             out  [L, D] bf16 (written)
@@ -183,7 +199,10 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that overlap on the GPU (different streams, no ordering) race.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine, and after
- *    the first call on a device creates no stream or event.                 */
+ *    the first call on a device creates no stream or event.  Its launches
+ *    record no profiling events even while upipe_profile_enable(1) is on
+ *    (recording may create events); they still count in
+ *    upipe_launch_count().                                                  */
 #define UPIPE_NOALLOC_SCRATCH_BYTES (32u << 20)
 int upipe_attn_core_bwd_noalloc(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq,

@@ -134,3 +134,96 @@ def test_32b_shape_u8_saves_87_5_percent(lib):
     full, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=64), 1)
     u8, _ = upipe.activation_bytes(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=8), 1)
     assert 1 - u8 / full == pytest.approx(0.875, abs=0)
+
+
+# --------------------------------------------------------- chunk-size choice
+
+def _valid_us(H, Hkv):
+    g = H // Hkv
+    return [u for u in range(1, H + 1) if H % u == 0 and (u % g == 0 or g % u == 0)]
+
+
+def _need(cfg, pass_):
+    if pass_ == 2:
+        return max(upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1))
+    return upipe.workspace_bytes(cfg, pass_)
+
+
+@pytest.mark.parametrize("pass_", [0, 1, 2])
+@pytest.mark.parametrize("L,D,H,Hkv", [(32768, 4096, 32, 8), (131072, 5120, 64, 8), (1024, 1024, 8, 2)])
+def test_choose_u_is_the_largest_fitting_chunk(lib, pass_, L, D, H, Hkv):
+    """At a budget equal to some U's workspace that U (or a larger one that
+    also fits) is chosen; one byte less never yields it."""
+    for u in _valid_us(H, Hkv):
+        cfg = upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=u)
+        need = _need(cfg, pass_)
+        fits = [v for v in _valid_us(H, Hkv) if _need(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=v), pass_) <= need]
+        assert upipe.choose_u(cfg, need, pass_) == max(fits)
+        below = [v for v in _valid_us(H, Hkv) if _need(upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=v), pass_) < need]
+        if below:
+            assert upipe.choose_u(cfg, need - 1, pass_) == max(below)
+
+
+def test_choose_u_budget_below_every_chunk_size(lib):
+    cfg = upipe.Config(L=32768, D=4096, H=32, Hkv=8, U=8)
+    smallest = min(_need(upipe.Config(L=32768, D=4096, H=32, Hkv=8, U=u), 2) for u in _valid_us(32, 8))
+    with pytest.raises(upipe.UpipeError) as e:
+        upipe.choose_u(cfg, smallest - 1)
+    assert e.value.code == upipe.UPIPE_ERR_WS_TOO_SMALL
+    assert upipe.choose_u(cfg, 1 << 62) == 32  # unlimited: the unchunked layer
+
+
+def test_choose_u_ignores_cfg_u_and_rejects_bad_arguments(lib):
+    a = upipe.Config(L=8192, D=4096, H=32, Hkv=8, U=3)  # U itself invalid: ignored
+    b = upipe.Config(L=8192, D=4096, H=32, Hkv=8, U=8)
+    budget = upipe.workspace_bytes(b, 1)
+    assert upipe.choose_u(a, budget, 1) == upipe.choose_u(b, budget, 1)
+    c = upipe.Config(L=8192, D=4096, H=32, Hkv=8, U=8).c()
+    assert lib.upipe_choose_u(ctypes.byref(c), 1 << 40, 3, 0, 0) == upipe.UPIPE_ERR_INVALID_ARG
+    assert lib.upipe_choose_u(None, 1 << 40, 2, 0, 0) == upipe.UPIPE_ERR_INVALID_ARG
+    bad = upipe.Config(L=8192, D=4096, H=30, Hkv=8, U=8).c()
+    assert lib.upipe_choose_u(ctypes.byref(bad), 1 << 40, 2, 0, 0) == upipe.UPIPE_ERR_INVALID_ARG
+
+
+def test_choose_u_picks_u8_for_the_32b_layer_at_its_workspace(lib):
+    """The 32B-shaped layer (L=131072): a budget of U=8's training-step
+    workspace selects U=8 (U=16 needs more)."""
+    cfg = upipe.Config(L=131072, D=5120, H=64, Hkv=8, U=8)
+    assert upipe.choose_u(cfg, _need(cfg, 2), 2) == 8
+
+
+# ------------------------------------------- argument checks of the binding
+
+def test_binding_rejects_mis_shaped_or_mis_typed_tensors_before_any_launch(lib):
+    """Shapes and dtypes of every tensor argument are checked in Python
+    before the library is called (CPU tensors: nothing can launch)."""
+    import torch
+    cfg = upipe.Config(L=64, H=4, Hkv=2, U=2)
+    q = torch.zeros(64, 4, 128, dtype=torch.bfloat16)
+    k = torch.zeros(64, 2, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(4, 64, dtype=torch.float32)
+    n0 = upipe.launch_count()
+    short_q = torch.zeros(63, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="q"):
+        upipe.attn_core_bwd(cfg, short_q, k, k, q, lse, q, q, k, k)
+    with pytest.raises(ValueError, match="lse"):
+        upipe.attn_core_bwd(cfg, q, k, k, q, lse[:, :32], q, q, k, k)
+    with pytest.raises(ValueError, match="o"):
+        upipe.attn_core_bwd_noalloc(cfg, q, k, k, q.float(), lse, q, q, k, k)
+    with pytest.raises(ValueError, match="v"):
+        upipe.attn_core_fwd(cfg, q, k, torch.zeros(64, 1, 128, dtype=torch.bfloat16), q, lse)
+    with pytest.raises(ValueError, match="CUDA"):
+        upipe.attn_core_fwd(cfg, q, k, k, q, lse)
+    lcfg = upipe.Config(L=64, D=256, H=4, Hkv=2, U=2)
+    x = torch.zeros(64, 256, dtype=torch.bfloat16)
+    w = torch.zeros(8 * 128, 256, dtype=torch.bfloat16)
+    wo = torch.zeros(256, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="x"):
+        upipe.attn_bwd(lcfg, x[:32], w, wo, x, lse, x, w.float(), wo.float())
+    with pytest.raises(ValueError, match="Wo"):
+        upipe.attn_bwd(lcfg, x, w, wo.t(), x, lse, x, w.float(), wo.float())
+    with pytest.raises(ValueError, match="o_saved"):
+        upipe.attn_bwd(lcfg, x, w, wo, x, lse, x, w.float(), wo.float(), o_saved=x)
+    with pytest.raises(ValueError, match="Wqkv"):
+        upipe.attn_fwd(lcfg, x, w[:512], wo, x, lse)
+    assert upipe.launch_count() == n0

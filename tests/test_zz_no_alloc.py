@@ -35,10 +35,17 @@ def test_noalloc_core_backward_matches_workspace_entry(L, H, Hkv, U):
     torch.cuda.synchronize()
     for call in range(2):
         outs = [torch.full_like(t, float("nan")) for t in ref]
+        torch.cuda.synchronize()
         before = torch.cuda.memory_allocated()
+        free_before = torch.cuda.mem_get_info()[0]
         upipe.attn_core_bwd_noalloc(cfg, q, k, v, o, lse, do, *outs)
         torch.cuda.synchronize()
         assert torch.cuda.memory_allocated() == before
+        if call == 1:
+            # The first call may create the library's second stream; after
+            # it, the device's free memory (which also sees allocations made
+            # inside the library, outside torch's allocator) must not move.
+            assert torch.cuda.mem_get_info()[0] == free_before, "the call allocated device memory"
         status_ok()
         for name, got, want in zip(("dq", "dk", "dv"), outs, ref):
             assert_close(f64(got), f64(want), f"{name} (call {call})")
