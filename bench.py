@@ -4,14 +4,17 @@
 One step = upipe_attn_fwd + upipe_attn_bwd of a GQA/RoPE causal attention
 layer (projections, RoPE, attention, output projection; forward and
 backward with per-chunk recomputation) on synthetic bf16 inputs resident in
-HBM.  Default workload: the Llama-3-8B layer shape (L=32768, D=4096, H=32,
-Hkv=8, d=128) with U=8 query heads per chunk.
+HBM.  Default workload: the 32B-shaped layer (L=131072, D=5120, H=64, Hkv=8,
+d=128) with U=8 query heads per chunk.
 
 Prints one JSON line.  `value` is the layer's algorithmic TFLOP/s (causal
 attention fwd+bwd 7*L^2*H*d plus the projections' 3*(2*L*D*(H+2Hkv)*d +
 2*L*H*d*D); the backward recomputation is hardware work and is not counted)
-over the device-timed steps.  `--impl reference` times the fp64 CPU oracle
-on the same metric instead.
+over the device-timed steps, which run with per-launch timing off; a
+separate profiled step gives the per-kernel table, the attention-only
+figure and the roofline.  A U sweep measures each chunk size's workspace
+high-water mark on the device next to the library's own arithmetic.
+`--impl reference` times the fp64 CPU oracle on the same metric instead.
 """
 
 from __future__ import annotations
@@ -20,6 +23,8 @@ import argparse
 import hashlib
 import json
 import os
+import re
+import socket
 import statistics
 import subprocess
 import sys
@@ -34,12 +39,26 @@ sys.path.insert(0, ROOT)
 METRIC = "causal attn fwd+bwd TFLOP/s (% BF16 peak) at 1 GB300; peak activation bytes vs U"
 
 WORKLOADS = {
+    "qwen32b_layer_L131072_U8": dict(L=131072, D=5120, H=64, Hkv=8, U=8),
     "llama3_8b_layer_L32768_U8": dict(L=32768, D=4096, H=32, Hkv=8, U=8),
     "tiny_L1024_U2": dict(L=1024, D=1024, H=8, Hkv=2, U=2),
-    "qwen32b_layer_L131072_U8": dict(L=131072, D=5120, H=64, Hkv=8, U=8),
     "llama3_8b_layer_L65536_U4": dict(L=65536, D=4096, H=32, Hkv=8, U=4),
+    "llama3_8b_layer_L262144_U4": dict(L=262144, D=4096, H=32, Hkv=8, U=4),
 }
-DEFAULT = "llama3_8b_layer_L32768_U8"
+DEFAULT = "qwen32b_layer_L131072_U8"
+# Chunk sizes measured by the U sweep (the workload's U among them).
+U_SWEEP = {
+    "qwen32b_layer_L131072_U8": (64, 16, 8),
+    "llama3_8b_layer_L32768_U8": (32, 8, 4),
+    "tiny_L1024_U2": (8, 4, 2),
+    "llama3_8b_layer_L65536_U4": (32, 8, 4),
+    "llama3_8b_layer_L262144_U4": (32, 8, 4),
+}
+TARGET_FRAC_OF_BURST = 0.55
+# Kernel kinds that are not attention: they run one at a time on the
+# caller's stream, so their event times add up to the step's projection time.
+PROJ_KINDS = ("rope_table", "qkv_gemm", "oproj_gemm", "do_gemm", "dwo_gemm", "dwqkv_gemm", "dx_gemm", "delta",
+              "zero_rows")
 
 
 def layer_flops(L, D, H, Hkv, d=128):
@@ -200,13 +219,22 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def strip_comments(text):
+    """C/C++ source without its comments and blank-line noise, so that a
+    comment-only edit does not invalidate a stored capture."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_sha(name):
     """Hash of a kernel's source file together with the headers every kernel
-    includes, so that a change to either invalidates a stored capture."""
+    includes (comments removed), so that a change to the code of either
+    invalidates a stored capture."""
     h = hashlib.sha256()
     for f in (name, "sm103_ptx.cuh", "upipe_internal.h"):
-        with open(os.path.join(ROOT, "headwise_chunked_context_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "headwise_chunked_context_gb300", "csrc", f)) as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -233,6 +261,60 @@ def traffic_for(kind, workload):
     return e.get("bytes_per_launch")
 
 
+def _bytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def u_sweep(w, u_list, dev, stream, x, wqkv, wo, dout, n_timed=1):
+    """For each chunk size U: the workspace high-water mark measured on the
+    device around the allocating helpers (torch.cuda.max_memory_allocated
+    minus the caller-visible outputs), next to the library's arithmetic
+    (chunk bytes scale with U, fixed bytes do not), and the step time."""
+    from headwise_chunked_context_gb300 import upipe
+    L, D, H, Hkv = w["L"], w["D"], w["H"], w["Hkv"]
+    rows = []
+    attn_f, proj_f = layer_flops(L, D, H, Hkv)
+    for u in u_list:
+        cfg = upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=u)
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        out, lse, _ = upipe.layer_forward(cfg, x, wqkv, wo)
+        torch.cuda.synchronize(dev)
+        fwd_peak = torch.cuda.max_memory_allocated(dev) - base - _bytes(out, lse)
+        base2 = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        dx, dw, dwo = upipe.layer_backward(cfg, x, wqkv, wo, dout, lse)
+        torch.cuda.synchronize(dev)
+        bwd_peak = torch.cuda.max_memory_allocated(dev) - base2 - _bytes(dx, dw, dwo)
+        ws = torch.empty(max(upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1)), dtype=torch.uint8,
+                         device=dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_timed):
+            upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
+            upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dw, dwo, None, ws, stream)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a0.elapsed_time(a1) / n_timed
+        cf, ff = upipe.activation_bytes(cfg, 0)
+        cb, fb = upipe.activation_bytes(cfg, 1)
+        rows.append({"U": u, "workspace_fwd_measured": fwd_peak, "workspace_bwd_measured": bwd_peak,
+                     "workspace_fwd": upipe.workspace_bytes(cfg, 0), "workspace_bwd": upipe.workspace_bytes(cfg, 1),
+                     "chunk_bytes_fwd": cf, "fixed_bytes_fwd": ff, "chunk_bytes_bwd": cb, "fixed_bytes_bwd": fb,
+                     "ms_per_step": ms, "tflops": (attn_f + proj_f) / (ms / 1e3) / 1e12})
+        del out, lse, dx, dw, dwo, ws
+    full = [r for r in rows if r["U"] == H]
+    if full:
+        for r in rows:
+            r["chunk_bytes_bwd_vs_unchunked"] = r["chunk_bytes_bwd"] / full[0]["chunk_bytes_bwd"]
+            r["chunk_saving_vs_unchunked"] = 1.0 - r["chunk_bytes_bwd_vs_unchunked"]
+    torch.cuda.empty_cache()
+    return rows
+
+
 def run_upipe(args, w, world, rank, local):
     from headwise_chunked_context_gb300 import upipe, build
     if not os.path.exists(upipe.LIB_PATH):
@@ -257,8 +339,6 @@ def run_upipe(args, w, world, rank, local):
     ws_bytes = max(upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)
-    base_alloc = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
 
     def step():
         upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
@@ -269,18 +349,21 @@ def run_upipe(args, w, world, rank, local):
             import torch.distributed as dist
             dist.barrier()
 
+    def check_status(when):
+        code = upipe.last_device_status(stream)
+        if code != 0:
+            raise RuntimeError(f"device status {when}: {upipe.strerror(code)}")
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    code = upipe.last_device_status(stream)
-    if code != 0:
-        raise RuntimeError(f"device status after warm-up: {upipe.strerror(code)}")
+    check_status("after warm-up")
 
-    # ---- timed region: K steps, device events, clocks sampled throughout
+    # ---- timed region: K steps, device events, clocks sampled throughout;
+    # no per-launch events are recorded here.
     barrier()
     torch.cuda.synchronize(dev)
     n0 = upipe.launch_count()
-    upipe.profile_enable(True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
@@ -289,19 +372,25 @@ def run_upipe(args, w, world, rank, local):
             step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-    upipe.profile_enable(False)
     launches = upipe.launch_count() - n0
     barrier()
     ms = e0.elapsed_time(e1)
-    prof = upipe.profile_read()
     clocks = clk.summary()
-    code = upipe.last_device_status(stream)
-    if code != 0:
-        raise RuntimeError(f"device status after timed steps: {upipe.strerror(code)}")
+    check_status("after the timed steps")
     ms = max_over_ranks(ms, dev)
-    peak_alloc = torch.cuda.max_memory_allocated(dev) - base_alloc
 
-    # ---- forward and backward timed separately, after the step timing
+    # ---- profiled pass (separate from the timing): per-launch event pairs
+    # on the launching streams.
+    n_prof = max(1, min(args.steps, 2))
+    upipe.profile_enable(True)
+    for _ in range(n_prof):
+        step()
+    torch.cuda.synchronize(dev)
+    upipe.profile_enable(False)
+    prof = upipe.profile_read()
+    check_status("after the profiled steps")
+
+    # ---- forward and backward timed separately
     def timed(fn, n):
         fn()
         torch.cuda.synchronize(dev)
@@ -316,9 +405,7 @@ def run_upipe(args, w, world, rank, local):
     n_split = max(1, min(args.steps, 3))
     fwd_ms = timed(lambda: upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream), n_split)
     bwd_ms = timed(lambda: upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream), n_split)
-    code = upipe.last_device_status(stream)
-    if code != 0:
-        raise RuntimeError(f"device status after the fwd/bwd split: {upipe.strerror(code)}")
+    check_status("after the fwd/bwd split")
 
     attn_f, proj_f = layer_flops(L, D, H, Hkv)
     step_flops = attn_f + proj_f
@@ -329,10 +416,10 @@ def run_upipe(args, w, world, rank, local):
     value = job_tflops(step_flops, ms_step, world)
     burst, sustained, hbm, peak_src = peaks()
 
-    # ---- roofline of the dominant kernel, from the live per-launch events.
-    # dQ runs concurrently with dK/dV on the caller's stream; its event pair
-    # opens at the fork, so its interval also holds the time its CTAs waited
-    # behind dK/dV's for SMs: it is reported as an interval, not a duration.
+    # ---- per-kernel table and roofline of the dominant kernel, from the
+    # profiled pass.  dQ runs concurrently with dK/dV on the caller's stream;
+    # its event pair opens at the fork, so its interval also holds the time
+    # its CTAs waited behind dK/dV's for SMs: it is reported as an interval.
     busy = {k: v for k, v in prof.items() if v[1] > 0}
     solo = {k: v for k, v in busy.items() if k not in OVERLAPPED}
     dom = max(solo, key=lambda k: solo[k][0])
@@ -342,17 +429,26 @@ def run_upipe(args, w, world, rank, local):
     traffic = traffic_for(dom, args.workload)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                 "frac": achieved / sustained, "traffic": traffic, "kernel": dom,
-                "peak_kind": f"bf16 sustained ({peak_src})"}
-    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps,
-                   "share_of_step": v[0] / args.steps / ms_step} for k, v in solo.items()}
+                "peak_kind": f"bf16 sustained ({peak_src}): the kernel is timed inside a long step",
+                "frac_of_burst": achieved / burst}
+    prof_step_ms = sum(v[0] for k, v in busy.items() if k not in OVERLAPPED) / n_prof
+    kernels = {k: {"ms_per_step": v[0] / n_prof, "launches_per_step": v[1] / n_prof,
+                   "share_of_step": v[0] / n_prof / ms_step} for k, v in solo.items()}
     for k in kernels:
         f = kernel_flops(k, w)
         if f:
             kernels[k]["tflops"] = f / (busy[k][0] / busy[k][1] / 1e3) / 1e12
     for k, other in OVERLAPPED.items():
         if k in busy:
-            kernels[k] = {"interval_ms_per_step": busy[k][0] / args.steps,
-                          "launches_per_step": busy[k][1] / args.steps, "concurrent_with": other}
+            kernels[k] = {"interval_ms_per_step": busy[k][0] / n_prof,
+                          "launches_per_step": busy[k][1] / n_prof, "concurrent_with": other}
+    # Attention alone: the step's time less the projection-side kernels
+    # (which run one at a time on the caller's stream).
+    proj_ms = sum(busy[k][0] for k in PROJ_KINDS if k in busy) / n_prof
+    attn_ms = ms_step - proj_ms
+    attention = {"tflops": world * attn_f / (attn_ms / 1e3) / 1e12, "ms_per_step": attn_ms,
+                 "flops_per_step": attn_f, "frac_of_burst": attn_f / (attn_ms / 1e3) / 1e12 / burst,
+                 "note": "7 L^2 H d over the step time less the projection kernels' event time"}
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -361,9 +457,9 @@ def run_upipe(args, w, world, rank, local):
         hx, hw, hwo, hd = pin(x), pin(wqkv), pin(wo), pin(dout)
         ho, hl, hdx, hdw, hdwo = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                                   for t in (out, lse, dx, dwqkv, dwo))
-        h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hwo, hd))
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdx, hdw, hdwo))
-        k_e2e = max(1, min(args.steps, 3))
+        h2d = _bytes(hx, hw, hwo, hd)
+        d2h = _bytes(ho, hl, hdx, hdw, hdwo)
+        k_e2e = max(3, min(args.steps, 10))
 
         # Copies that the layer does not wait for run on a second stream:
         # dout streams in during the forward, out and LSE stream back during
@@ -402,27 +498,27 @@ def run_upipe(args, w, world, rank, local):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a0.elapsed_time(a1) / k_e2e
+        e2e_ms = max_over_ranks(a0.elapsed_time(a1) / k_e2e, dev)
         e2e = {"value": world * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": k_e2e}
+        del hx, hw, hwo, hd, ho, hl, hdx, hdw, hdwo
 
-    # ---- activation accounting vs U
-    act = {}
-    for u in sorted({U, H}):
-        c = upipe.Config(L=L, D=D, H=H, Hkv=Hkv, U=u)
-        fb, ff = upipe.activation_bytes(c, 0)
-        bb, bf = upipe.activation_bytes(c, 1)
-        act[f"U={u}"] = {"chunk_bytes_fwd": fb, "chunk_bytes_bwd": bb, "fixed_bytes_bwd": bf,
-                         "workspace_bwd": upipe.workspace_bytes(c, 1)}
+    # ---- peak activation bytes and throughput against U (measured)
+    del ws
+    sweep = None
+    if not args.no_u_sweep:
+        sweep = u_sweep(w, U_SWEEP.get(args.workload, (H, U)), dev, stream, x, wqkv, wo, dout)
+        check_status("after the U sweep")
 
     if rank != 0:
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        v, s = cpu_oracle_sample(L)
+        Ls = min(L, args.cpu_sample_L)
+        v, s = cpu_oracle_sample(Ls)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"fp64 NumPy oracle, one query head (H=Hkv=1) of causal attention fwd+bwd at L={L}, "
-                         f"{s:.1f} s"}
+               "sample": f"fp64 NumPy oracle, one query head (H=Hkv=1) of causal attention fwd+bwd at L={Ls} "
+                         f"(BLAS threads: all {os.cpu_count()} host cores), {s:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -433,30 +529,50 @@ def run_upipe(args, w, world, rank, local):
                           else f"inputs fit in L2 (x, dout {L * D * 2 / 2**20:.1f} MiB each; not flushed)"),
                    "parallelism": f"replicas x{world}"},
         "pct_bf16_peak": {"burst": value / world / burst, "sustained": value / world / sustained,
-                          "peaks": f"{burst}/{sustained} TFLOP/s ({peak_src})"},
+                          "target_of_burst": TARGET_FRAC_OF_BURST,
+                          "peaks": f"{burst} burst / {sustained} sustained TFLOP/s ({peak_src})"},
+        "attention_only": attention,
         "fwd_bwd": {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                     "fwd_tflops": world * (attn_f * 2.0 / 7.0 + proj_f / 3.0) / (fwd_ms / 1e3) / 1e12,
                     "bwd_tflops": world * (attn_f * 5.0 / 7.0 + proj_f * 2.0 / 3.0) / (bwd_ms / 1e3) / 1e12},
         "hfu": {"value": world * (step_flops + recompute_flops) / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
                 "note": "hardware flops: the layer flops plus the backward's recompute of QKV and attention fwd"},
-        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks, "activation_bytes": act, "peak_alloc_bytes_in_step": peak_alloc,
+        "roofline": roofline, "kernels": kernels, "profiled_step_ms": prof_step_ms,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks, "u_sweep": sweep,
     }
     print(json.dumps(line), flush=True)
 
 
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="world size: ranks (one per GPU); without torchrun, N > 1 relaunches under it")
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="upipe", choices=["upipe", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--ref-sample-L", type=int, default=8192)
+    ap.add_argument("--cpu-sample-L", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-u-sweep", action="store_true")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
-    world, rank, local = (1, 0, 0)
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        # --gpus drives the world size: one process per GPU under torchrun.
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__),
+               *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
+    if env_world is not None and int(env_world) != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but WORLD_SIZE={env_world}: they must agree")
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
