@@ -40,13 +40,22 @@ Every function below is plain: library matmuls and elementwise NumPy, no
 blocking beyond streaming query rows against the full K/V (which changes no
 arithmetic that matters at fp64), no fusion.
 
-Precision model ("bf16 in / fp32 accumulate").  By default everything is
-exact fp64.  With ``bf16_tensors=True`` the layer functions round, at the
-points where a bf16 implementation stores them, the tensors that are bf16
-inputs of the next contraction -- Q and K after RoPE, V, the attention output
-O, and dO = dout Wo -- to the nearest bfloat16 (``bf16_round``); every
-product and sum stays exact fp64.  This isolates an implementation's own
-arithmetic from the rounding that the bf16 storage itself implies.
+Precision model ("bf16 in / fp32 accumulate", the stated tolerance's
+precision).  By default everything is exact fp64.  With
+``bf16_operands=True`` every input of every contraction of the definition is
+rounded to the nearest bfloat16 (``bf16_round``) -- that is what "bf16 in"
+says -- while every product, sum and element-wise step stays exact fp64
+(better than the fp32 the model allows):
+
+* stored tensors that feed the next contraction: Q and K after RoPE, V, the
+  attention output O, and dO = dout Wo;
+* the softmax tiles where they enter a product: the probabilities
+  P = exp(S - LSE) in P V (forward) and in P^T dO (backward), and
+  dS = P * (dP - Delta) in dS K and dS^T Q.  P inside dS's element-wise
+  formula is not a contraction input and stays exact.
+
+This isolates an implementation's own arithmetic (accumulation order, fp32
+element-wise math) from the rounding the precision model itself implies.
 """
 
 from __future__ import annotations
@@ -129,16 +138,29 @@ def project_qkv(x, Wqkv, H, Hkv, d, theta, rope=True):
 # Exact causal attention, one query head at a time.
 # ---------------------------------------------------------------------------
 
+# Query rows per streamed block.  None sizes blocks so that one block's
+# score matrix stays near 64 MB; tests set a small value to run the
+# multi-block path on small inputs.
+ROW_BLOCK = None
+
+
 def _row_block(n: int, L: int) -> int:
-    # Stream query rows so that one block's score matrix stays near 64 MB.
+    if ROW_BLOCK is not None:
+        return max(1, min(n, int(ROW_BLOCK)))
     return max(1, min(n, (8 << 20) // max(L, 1)))
 
 
-def attention_head_rows(qr, qpos, k, v, scale):
+def _op(a, bf16_operands):
+    """A contraction input under the precision model (module header)."""
+    return bf16_round(a) if bf16_operands else a
+
+
+def attention_head_rows(qr, qpos, k, v, scale, bf16_operands=False):
     """O rows and LSE for query rows ``qr`` [n, d] at positions ``qpos``.
 
     ``k``, ``v`` [Lk, d] are this head's keys/values (KV head h // g).
-    Key j is visible to the query at position p iff j <= p.
+    Key j is visible to the query at position p iff j <= p.  With
+    ``bf16_operands`` the probabilities exp(S - LSE) enter P V as bf16.
     """
     qr = np.asarray(qr, dtype=F64)
     qpos = np.asarray(qpos)
@@ -153,14 +175,14 @@ def attention_head_rows(qr, qpos, k, v, scale):
         mask = np.arange(top)[None, :] > qpos[s0:s1, None]
         S[mask] = -np.inf
         m = S.max(axis=1)
-        P = np.exp(S - m[:, None])
-        l = P.sum(axis=1)
-        o[s0:s1] = (P @ v[:top]) / l[:, None]
+        l = np.exp(S - m[:, None]).sum(axis=1)
         lse[s0:s1] = m + np.log(l)
+        P = np.exp(S - lse[s0:s1, None])
+        o[s0:s1] = _op(P, bf16_operands) @ v[:top]
     return o, lse
 
 
-def attention_core_fwd(q, k, v, causal=True):
+def attention_core_fwd(q, k, v, causal=True, bf16_operands=False):
     """O [L, H, d] and LSE [H, L] for q [L, H, d], k/v [L, Hkv, d]."""
     assert causal, "only the causal square mask is defined here"
     q = np.asarray(q, dtype=F64)
@@ -174,16 +196,18 @@ def attention_core_fwd(q, k, v, causal=True):
     lse = np.zeros((H, L), dtype=F64)
     pos = np.arange(L)
     for h in range(H):
-        o[:, h], lse[h] = attention_head_rows(q[:, h], pos, k[:, h // g], v[:, h // g], scale)
+        o[:, h], lse[h] = attention_head_rows(q[:, h], pos, k[:, h // g], v[:, h // g], scale, bf16_operands)
     return o, lse
 
 
-def attention_core_bwd(q, k, v, o, lse, do):
+def attention_core_bwd(q, k, v, o, lse, do, bf16_operands=False):
     """dq, dk, dv for the causal core, closed-form softmax backward.
 
     P = exp(S - LSE), dV = P^T dO, dP = dO V^T, Delta = rowsum(dO * O),
     dS = P * (dP - Delta), dQ = dS K * scale, dK = dS^T Q * scale.
-    dK/dV of a KV head sum over the g query heads that read it.
+    dK/dV of a KV head sum over the g query heads that read it.  With
+    ``bf16_operands`` P (in P^T dO) and dS (in dS K, dS^T Q) enter their
+    products as bf16.
     """
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -209,15 +233,15 @@ def attention_core_bwd(q, k, v, o, lse, do):
             mask = np.arange(top)[None, :] > np.arange(s0, s1)[:, None]
             P = np.exp(S - lse[h, s0:s1, None])
             P[mask] = 0.0
-            dv[:top, h // g] += P.T @ do[s0:s1, h]
+            dv[:top, h // g] += _op(P, bf16_operands).T @ do[s0:s1, h]
             dP = do[s0:s1, h] @ vh[:top].T
-            dS = P * (dP - delta[s0:s1, None])
+            dS = _op(P * (dP - delta[s0:s1, None]), bf16_operands)
             dq[s0:s1, h] = (dS @ kh[:top]) * scale
             dk[:top, h // g] += (dS.T @ q[s0:s1, h]) * scale
     return dq, dk, dv
 
 
-def attention_dq_rows(qr, qpos, k, v, dor, orow, lser, scale):
+def attention_dq_rows(qr, qpos, k, v, dor, orow, lser, scale, bf16_operands=False):
     """dQ rows for sampled query rows of one head (needs only that row's
     O, dO and LSE: Delta_i = sum_k dO_ik O_ik)."""
     qr = np.asarray(qr, dtype=F64)
@@ -236,11 +260,11 @@ def attention_dq_rows(qr, qpos, k, v, dor, orow, lser, scale):
         P[mask] = 0.0
         delta = np.sum(dor[s0:s1] * orow[s0:s1], axis=1)
         dP = dor[s0:s1] @ v[:top].T
-        dq[s0:s1] = ((P * (dP - delta[:, None])) @ k[:top]) * scale
+        dq[s0:s1] = (_op(P * (dP - delta[:, None]), bf16_operands) @ k[:top]) * scale
     return dq
 
 
-def attention_dkv_tail(q_tail, k_tail, v_tail, do_tail, o_tail, lse_tail, scale):
+def attention_dkv_tail(q_tail, k_tail, v_tail, do_tail, o_tail, lse_tail, scale, bf16_operands=False):
     """dK, dV of the last T keys of one head pair, from the last T queries.
 
     Under the causal mask only queries at or after a key's position reach
@@ -259,36 +283,34 @@ def attention_dkv_tail(q_tail, k_tail, v_tail, do_tail, o_tail, lse_tail, scale)
     P[mask] = 0.0
     delta = np.sum(do_tail * o_tail, axis=1)
     dP = do_tail @ v_tail.T
-    dS = P * (dP - delta[:, None])
-    return (dS.T @ q_tail) * scale, P.T @ do_tail
+    dS = _op(P * (dP - delta[:, None]), bf16_operands)
+    return (dS.T @ q_tail) * scale, _op(P, bf16_operands).T @ do_tail
 
 
 # ---------------------------------------------------------------------------
 # The layer: plain (all heads at once) definition.
 # ---------------------------------------------------------------------------
 
-def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None, bf16_tensors=False):
+def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None, bf16_operands=False):
     """out [L, D], LSE [H, L], O [L, H, d] of one GQA/RoPE attention layer."""
     x = np.asarray(x, dtype=F64)
     Wo = np.asarray(Wo, dtype=F64)
     if d is None:
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
-    if bf16_tensors:
-        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
-    o, lse = attention_core_fwd(q, k, v)
-    if bf16_tensors:
-        o = bf16_round(o)
+    q, k, v = _op(q, bf16_operands), _op(k, bf16_operands), _op(v, bf16_operands)
+    o, lse = attention_core_fwd(q, k, v, bf16_operands=bf16_operands)
+    o = _op(o, bf16_operands)
     out = o.reshape(x.shape[0], H * d) @ Wo.T
     return out, lse, o
 
 
-def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_tensors=False):
+def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_operands=False):
     """dx [L, D], dWqkv [(H+2Hkv)d, D], dWo [D, H d]: gradient of sum(out*dout).
 
-    With ``bf16_tensors`` the gradient is the one of the bf16-materialised
-    layer (see the module header): Q, K, V, O and dO are rounded to bf16
-    where they are stored; the rounding itself is treated as the identity.
+    With ``bf16_operands`` every contraction input is rounded to bf16 (see
+    the module header); the rounding itself is treated as the identity in
+    the chain rule.
     """
     x = np.asarray(x, dtype=F64)
     Wqkv = np.asarray(Wqkv, dtype=F64)
@@ -298,17 +320,13 @@ def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_tensors=False):
     if d is None:
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
-    if bf16_tensors:
-        q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
-    o, lse = attention_core_fwd(q, k, v)
-    if bf16_tensors:
-        o = bf16_round(o)
+    q, k, v = _op(q, bf16_operands), _op(k, bf16_operands), _op(v, bf16_operands)
+    o, lse = attention_core_fwd(q, k, v, bf16_operands=bf16_operands)
+    o = _op(o, bf16_operands)
     o_flat = o.reshape(L, H * d)
     dWo = dout.T @ o_flat
-    do = (dout @ Wo).reshape(L, H, d)
-    if bf16_tensors:
-        do = bf16_round(do)
-    dq, dk, dv = attention_core_bwd(q, k, v, o, lse, do)
+    do = _op((dout @ Wo).reshape(L, H, d), bf16_operands)
+    dq, dk, dv = attention_core_bwd(q, k, v, o, lse, do, bf16_operands=bf16_operands)
     pos = np.arange(L)
     dq = rope_apply(dq, pos, theta, inverse=True)
     dk = rope_apply(dk, pos, theta, inverse=True)

@@ -345,21 +345,144 @@ def test_bf16_round_matches_library_conversion():
     assert orc.bf16_round(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
 
 
-def test_bf16_materialised_layer_is_the_exact_layer_on_rounded_tensors():
-    """With bf16_tensors the forward equals the exact forward fed with the
-    rounded Q/K/V and rounded O, and differs from the exact layer only at the
-    bf16 level."""
+def _bf(a):
+    """bf16 rounding through torch's own conversion (independent of
+    orc.bf16_round)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).float().to(torch.bfloat16).double().numpy()
+
+
+def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs():
+    """With bf16_operands the layer equals a restatement written here from
+    the definition, whose every contraction input (Q, K, V after RoPE, P in
+    P V and P^T dO, O, dO, dS in dS K and dS^T Q) goes through torch's bf16
+    conversion, with all else exact; and it differs from the exact layer
+    only at the bf16 level."""
     x, Wqkv, Wo, dout, H, Hkv, theta = _micro(seed=3, L=24, D=32)
-    out_b, lse_b, o_b = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta, bf16_tensors=True)
+    L = x.shape[0]
     d = Wo.shape[1] // H
-    q, k, v = orc.project_qkv(x, Wqkv, H, Hkv, d, theta)
-    o, lse = orc.attention_core_fwd(orc.bf16_round(q), orc.bf16_round(k), orc.bf16_round(v))
+    g = H // Hkv
+    sc = 1 / math.sqrt(d)
+    out_b, lse_b, o_b = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta, bf16_operands=True)
+    dx_b, dW_b, dWo_b = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, bf16_operands=True)
+    q, k, v = (_bf(t) for t in orc.project_qkv(x, Wqkv, H, Hkv, d, theta))
+    o = np.zeros((L, H, d))
+    lse = np.zeros((H, L))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    causal = np.tril(np.ones((L, L), dtype=bool))
+    for h in range(H):
+        S = q[:, h] @ k[:, h // g].T * sc
+        S[~causal] = -np.inf
+        lse[h] = logsumexp(S, axis=1)
+        P = np.exp(S - lse[h][:, None])
+        o[:, h] = _bf(P) @ v[:, h // g]
+    o = _bf(o)
+    do = _bf((dout @ Wo).reshape(L, H, d))
+    for h in range(H):
+        S = q[:, h] @ k[:, h // g].T * sc
+        P = np.where(causal, np.exp(S - lse[h][:, None]), 0.0)
+        delta = np.sum(do[:, h] * o[:, h], axis=1)
+        dS = _bf(P * (do[:, h] @ v[:, h // g].T - delta[:, None]))
+        dv[:, h // g] += _bf(P).T @ do[:, h]
+        dk[:, h // g] += dS.T @ q[:, h] * sc
+        dq[:, h] = dS @ k[:, h // g] * sc
     np.testing.assert_allclose(lse_b, lse, atol=1e-13)
-    np.testing.assert_allclose(out_b, orc.bf16_round(o).reshape(x.shape[0], -1) @ Wo.T, atol=1e-13)
+    np.testing.assert_allclose(o_b, o, atol=1e-13)
+    np.testing.assert_allclose(out_b, o.reshape(L, -1) @ Wo.T, atol=1e-13)
+    pos = np.arange(L)
+    dqkv = np.concatenate([orc.rope_apply(dq, pos, theta, inverse=True).reshape(L, -1),
+                           orc.rope_apply(dk, pos, theta, inverse=True).reshape(L, -1), dv.reshape(L, -1)], 1)
+    np.testing.assert_allclose(dx_b, dqkv @ Wqkv, atol=1e-12)
+    np.testing.assert_allclose(dW_b, dqkv.T @ x, atol=1e-12)
+    np.testing.assert_allclose(dWo_b, dout.T @ o.reshape(L, -1), atol=1e-12)
     out, _, _ = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta)
     rel = np.linalg.norm(out_b - out) / np.linalg.norm(out)
     assert 1e-5 < rel < 1e-2
-    dx_b, dW_b, dWo_b = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, bf16_tensors=True)
     dx, dW, dWo = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta)
-    for a, b in ((dx_b, dx), (dW_b, dW), (dWo_b, dWo)):
-        assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-2
+    for a_, b_ in ((dx_b, dx), (dW_b, dW), (dWo_b, dWo)):
+        assert 1e-6 < np.linalg.norm(a_ - b_) / np.linalg.norm(b_) < 1e-2
+
+
+# ------------------------------------------------- streamed query-row blocks
+#
+# The attention functions stream query rows in blocks (sized so one block's
+# scores stay near 64 MB).  At the sizes above every call is one block; the
+# tests below force several blocks, with a ragged last one, so that the
+# multi-block path (each block's mask offset and key range) is pinned too.
+
+@pytest.fixture
+def small_blocks(monkeypatch):
+    monkeypatch.setattr(orc, "ROW_BLOCK", 37)
+    assert orc._row_block(300, 300) == 37
+
+
+@pytest.mark.parametrize("L,H,Hkv,d", [(300, 4, 2, 16), (111, 2, 1, 8)])
+def test_multi_block_core_forward_matches_library_attention(small_blocks, L, H, Hkv, d):
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((L, H, d))
+    k = rng.standard_normal((L, Hkv, d))
+    v = rng.standard_normal((L, Hkv, d))
+    o, lse = orc.attention_core_fwd(q, k, v)
+    np.testing.assert_allclose(o, _sdpa_gqa(q, k, v), rtol=1e-11, atol=1e-12)
+    g = H // Hkv
+    for h in range(H):
+        S = q[:, h] @ k[:, h // g].T / math.sqrt(d)
+        S[np.triu_indices(L, 1)] = -np.inf
+        np.testing.assert_allclose(lse[h], logsumexp(S, axis=1), rtol=1e-13, atol=1e-12)
+
+
+@pytest.mark.parametrize("L,H,Hkv,d", [(300, 4, 2, 16), (111, 2, 1, 8)])
+def test_multi_block_core_backward_matches_torch_autograd(small_blocks, L, H, Hkv, d):
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((L, H, d))
+    k = rng.standard_normal((L, Hkv, d))
+    v = rng.standard_normal((L, Hkv, d))
+    do = rng.standard_normal((L, H, d))
+    o, lse = orc.attention_core_fwd(q, k, v)
+    dq, dk, dv = orc.attention_core_bwd(q, k, v, o, lse, do)
+    g = H // Hkv
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(
+        tq.permute(1, 0, 2)[None], tk.repeat_interleave(g, dim=1).permute(1, 0, 2)[None],
+        tv.repeat_interleave(g, dim=1).permute(1, 0, 2)[None], is_causal=True)[0].permute(1, 0, 2)
+    (to * torch.from_numpy(do)).sum().backward()
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_multi_block_results_equal_single_block(monkeypatch):
+    """Blocked and unblocked runs of every streamed function agree, in both
+    precision modes, including the sampled-row helpers at scattered rows."""
+    rng = np.random.default_rng(23)
+    L, H, Hkv, d = 257, 4, 1, 16
+    q = rng.standard_normal((L, H, d))
+    k = rng.standard_normal((L, Hkv, d))
+    v = rng.standard_normal((L, Hkv, d))
+    do = rng.standard_normal((L, H, d))
+    rows = np.array([0, 3, 40, 41, 128, 200, 256])
+    sc = 1 / math.sqrt(d)
+
+    def run(bf):
+        o, lse = orc.attention_core_fwd(q, k, v, bf16_operands=bf)
+        grads = orc.attention_core_bwd(q, k, v, o, lse, do, bf16_operands=bf)
+        ro, rl = orc.attention_head_rows(q[rows, 1], rows, k[:, 0], v[:, 0], sc, bf16_operands=bf)
+        rdq = orc.attention_dq_rows(q[rows, 1], rows, k[:, 0], v[:, 0], do[rows, 1], o[rows, 1], lse[1, rows], sc,
+                                    bf16_operands=bf)
+        return (o, lse, *grads, ro, rl, rdq)
+
+    for bf in (False, True):
+        monkeypatch.setattr(orc, "ROW_BLOCK", None)
+        one = run(bf)
+        monkeypatch.setattr(orc, "ROW_BLOCK", 5)
+        many = run(bf)
+        for a_, b_ in zip(one, many):
+            np.testing.assert_allclose(b_, a_, rtol=1e-12, atol=1e-12)
+
+
+def test_default_blocking_streams_long_sequences():
+    """Without an override, a long sequence is split into several blocks of
+    at most 8 Mi scores each (the branch the multi-block pins exercise)."""
+    assert orc.ROW_BLOCK is None
+    assert orc._row_block(1 << 20, 1 << 20) == 8
+    assert orc._row_block(131072, 131072) == 64
+    assert orc._row_block(300, 300) == 300
