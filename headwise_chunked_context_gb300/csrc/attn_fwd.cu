@@ -24,6 +24,18 @@
 //    and P(j) need not wait for P V of block j - 1.  O is rescaled in TMEM
 //    only when a row maximum grows by more than 2^8, which bounds every
 //    exponent and keeps the result exact up to rounding.
+//
+// Three modes (a template parameter):
+//  * kOnline: the online softmax above; writes O and LSE;
+//  * kLseIn: the row's LSE is given (the forward's), so every block's
+//    probabilities are final at once -- P = exp2(S log2(e)/sqrt(d) -
+//    LSE log2(e)), the softmax's own definition -- and O = sum_j P_j V_j
+//    needs no running maximum, rescaling, row sum or division.  The
+//    backward's recomputation of O uses it: its P is the P the backward
+//    kernels use, rounded to bf16 the same way;
+//  * kLseOnly: row maximum and sum only (no P V, no O), for a forward that
+//    keeps O for the backward and then writes it with kLseIn, so that a
+//    kept O and a recomputed O are the same bits.
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -63,9 +75,11 @@ constexpr int TM_S = 64;   // scores: [64, 192)
 constexpr int TM_O = 192;  // O accumulator: [192, 320)
 constexpr int TM_P = 320;  // two P buffers, packed bf16: [320, 384), [384, 448)
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ AttnFwdParams p) {
+  constexpr bool kWithPV = MODE != kLseOnly;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -132,11 +146,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + OFF_K + s * kTile, &mk, bar(B_K_FULL + s), 0, j * 128, kz);
         tma_load_3d(sb + OFF_K + s * kTile + kHalf, &mk, bar(B_K_FULL + s), 64, j * 128, kz);
         last_k[s] = j;
-        if (!mbar_wait(bar(B_V_EMPTY + s), ph ^ 1, w)) break;
-        mbar_expect_tx(bar(B_V_FULL + s), kTile);
-        tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, j * 128, vz);
-        tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, j * 128, vz);
-        last_v[s] = j;
+        if constexpr (kWithPV) {
+          if (!mbar_wait(bar(B_V_EMPTY + s), ph ^ 1, w)) break;
+          mbar_expect_tx(bar(B_V_FULL + s), kTile);
+          tma_load_3d(sb + OFF_V + s * kTile, &mv, bar(B_V_FULL + s), 0, j * 128, vz);
+          tma_load_3d(sb + OFF_V + s * kTile + kHalf, &mv, bar(B_V_FULL + s), 64, j * 128, vz);
+          last_v[s] = j;
+        }
       }
       if (*abort_flag) {  // let every issued copy land before the CTA exits
         mbar_wait_drain(bar(B_Q_FULL), 0, p.status);
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 6) {
     // ----------------------------------------------------------- PV issuer
-    if (lane == 0) {
+    if (kWithPV && lane == 0) {
       constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 1);  // P (TMEM) x V (smem, MN-major)
       bool ok = true;
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -200,6 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_use = -INFINITY;  // running max used as the exponent offset (log2 domain)
     float l = 0.f;
+    // kLseIn: -LSE * log2(e) of this row (0 past L: such rows are never stored).
+    const float nl = MODE == kLseIn && qpos < p.L
+                         ? -p.lse_in[static_cast<int64_t>(h) * p.L + qpos] * 1.4426950408889634074f
+                         : 0.f;
     // Q row r -> TMEM (packed bf16, element pairs per column).
     bool ok = warp_wait(bar(B_Q_FULL), 0, w);
     if (ok) {
@@ -252,6 +272,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) x[c] = -INFINITY;
       }
+      if constexpr (MODE == kLseIn) {
+        // Final probabilities at once: P = exp2(S sl2 - LSE log2(e)).
+        uint32_t pk0[32], pk1[32];
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t nlx2 = f2_pack(nl, nl);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float t0, t1, t2, t3;
+          f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sl2x2, nlx2), t0, t1);
+          f2_unpack(f2_fma(f2_pack(x[64 + c], x[64 + c + 1]), sl2x2, nlx2), t2, t3);
+          pk0[c >> 1] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+          pk1[c >> 1] = pack_bf16x2(ex2_approx(t2), ex2_approx(t3));
+        }
+        if (j >= 2) {
+          if (!(ok = warp_wait(bar(B_P_EMPTY + b), ((j >> 1) & 1) ^ 1, w))) break;
+          tc_fence_after();
+        }
+        tmem_st32(trow + TM_P + b * 64 + 0, pk0);
+        tmem_st32(trow + TM_P + b * 64 + 32, pk1);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
+        continue;
+      }
       // Row max: four independent chains of 3-input max.
       float mc[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
@@ -266,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
       const float m_new = fmaxf(m_use, mx * sl2);
       const bool need = m_new > m_use + 8.0f;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      if (kWithPV && j > 0 && __any_sync(0xffffffffu, need)) {
         // O holds PV(0..j-1) once PV(j - 1) completes: rescale the rows
         // that moved.
         if (!(ok = warp_wait(bar(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, w))) break;
@@ -282,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(trow + TM_O + c4 * 32, o);
         }
         l *= f;
+      } else if (!kWithPV && need) {
+        l *= ex2_approx(m_use - m_new);  // no O to rescale: only the row sum
       }
       if (need) m_use = m_new;
 
@@ -309,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rs += a + b;
       }
       l += rs;
+      if constexpr (!kWithPV) continue;
       // P buffer b held P(j - 2) until PV(j - 2) completed.
       if (j >= 2) {
         if (!(ok = warp_wait(bar(B_P_EMPTY + b), ((j >> 1) & 1) ^ 1, w))) break;
@@ -322,10 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
     }
     // PV products complete in issue order: the last one completing means O is final.
-    if (ok) ok = warp_wait(bar(B_P_EMPTY + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, w);
-    if (ok) {
+    if (kWithPV && ok) ok = warp_wait(bar(B_P_EMPTY + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1, w);
+    if (ok && !kWithPV) {
+      if (qpos < p.L) p.lse[static_cast<int64_t>(h) * p.L + qpos] = (m_use + log2f(l)) * 0.69314718055994530942f;
+    } else if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = MODE == kLseIn ? 1.f : 1.f / l;
       const bool valid = qpos < p.L;
       __nv_bfloat16* orow = p.o + static_cast<int64_t>(qpos) * p.o_row + static_cast<int64_t>(h) * p.o_head;
 #pragma unroll
@@ -344,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && p.write_lse)
+      if (MODE == kOnline && valid && p.write_lse)
         p.lse[static_cast<int64_t>(h) * p.L + qpos] = (m_use + log2f(l)) * 0.69314718055994530942f;
     }
     tc_fence_before();
@@ -357,15 +407,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnFwdParams& p,
+                        int n_qblocks, cudaStream_t s) {
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_qblocks * p.nheads);
+  attn_fwd_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_attn_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const AttnFwdParams& p, int n_qblocks, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid(n_qblocks * p.nheads);
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(q, k, v, p);
-  return cudaGetLastError();
+  switch (p.mode) {
+    case kOnline: return launch_mode<kOnline>(q, k, v, p, n_qblocks, s);
+    case kLseIn: return launch_mode<kLseIn>(q, k, v, p, n_qblocks, s);
+    case kLseOnly: return launch_mode<kLseOnly>(q, k, v, p, n_qblocks, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace upipe

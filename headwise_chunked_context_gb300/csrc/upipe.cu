@@ -425,7 +425,9 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     g.rope = rope;
     UPIPE_LAUNCH(UPIPE_KIND_QKV_GEMM, launch_gemm(GK_QKV, m_x, m_wqkv, g, st));
 
-    // a-3: causal attention.
+    // a-3: causal attention.  A kept O is written from the final
+    // probabilities (LSE first, then O from it): the same bits the
+    // backward's recomputation of O produces.
     AttnFwdParams a;
     std::memset(&a, 0, sizeof(a));
     a.L = static_cast<int>(L);
@@ -442,6 +444,13 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
     a.status = status;
     a.limit_ns = limit;
+    if (o_saved) {
+      a.mode = kLseOnly;
+      UPIPE_LAUNCH(UPIPE_KIND_ATTN_FWD, launch_attn_fwd(m_qkv, m_qkv, m_qkv, a, m_tiles, st));
+      a.mode = kLseIn;
+      a.lse_in = a.lse;
+      a.write_lse = 0;
+    }
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_FWD, launch_attn_fwd(m_qkv, m_qkv, m_qkv, a, m_tiles, st));
 
     // a-4: out32 (+)= O_c Wo[:, cols_c]^T; the last chunk writes bf16 out.
@@ -536,10 +545,14 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     g.rope = rope;
     UPIPE_LAUNCH(UPIPE_KIND_QKV_GEMM, launch_gemm(GK_QKV, m_x, m_wqkv, g, st));
 
-    // Recompute O_c unless the caller kept it (a-3).
+    // Recompute O_c unless the caller kept it (a-3), from the forward's LSE:
+    // the probabilities are final at once, and are the ones the backward
+    // kernels use.
     if (!o_saved) {
       AttnFwdParams a;
       std::memset(&a, 0, sizeof(a));
+      a.mode = kLseIn;
+      a.lse_in = lse + static_cast<int64_t>(ch.q0) * L;
       a.L = static_cast<int>(L);
       a.nheads = s.U;
       a.g_loc = s.U / s.kvc;

@@ -62,15 +62,24 @@ struct GemmParams {
 //
 // Q, K, V (and dO) are read through 3-D tensor maps {d, L, heads}; the z
 // coordinate of local head h is q_z0 + h, of its KV head k_z0 + h / g_loc.
+// Forward attention modes (see attn_fwd.cu).
+enum AttnFwdMode : int {
+  kOnline = 0,   // online softmax: O and LSE
+  kLseIn = 1,    // LSE given (lse_in): O from the final probabilities
+  kLseOnly = 2,  // LSE only
+};
+
 struct AttnFwdParams {
+  int mode;     // AttnFwdMode
   int L;
   int nheads;   // query heads in this launch
   int g_loc;    // query heads per KV head in this launch
   int q_z0, k_z0, v_z0;
   __nv_bfloat16* o;  // O of local head h, row p: o + p*o_row + h*o_head
   int64_t o_row, o_head;
-  float* lse;        // [nheads, L]; not written when write_lse == 0
+  float* lse;        // [nheads, L]; kOnline (when write_lse) and kLseOnly write it
   int write_lse;
+  const float* lse_in;  // kLseIn: [nheads, L], natural log
   float scale_log2;  // log2(e) / sqrt(d)
   int* status;
   uint64_t limit_ns;

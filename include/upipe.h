@@ -147,6 +147,11 @@ int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core
  *   o_saved  [L, H*128] bf16 or NULL: when given, the attention output O is
  *            written there (and may be passed to upipe_attn_bwd to skip the
  *            recomputation of O); when NULL, O lives only in the workspace.
+ *            A kept O is computed from the final softmax probabilities
+ *            (each row's LSE first, then O = sum_j exp(S_j - LSE) V_j), the
+ *            same bits the backward's recomputation produces, so both
+ *            backward variants return identical gradients; this costs the
+ *            forward one more pass over the keys.
  *   ws       workspace of at least upipe_workspace_bytes(cfg, 0, 0, o_saved != NULL) */
 int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
                    uint16_t* out, float* lse, uint16_t* o_saved, void* ws, size_t ws_bytes, void* stream);

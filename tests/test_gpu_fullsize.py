@@ -1,17 +1,20 @@
 """GPU parity at the full workload sizes, on outputs the fp64 oracle can
 compute one by one, plus bit-exactness of every chunk size U at those sizes.
 
-Sampled checks (oracle fp64 in its bf16-materialisation mode: Q, K, V, O
-and dO rounded to bf16 where a bf16 layer stores them; the GPU run is the
+Sampled checks (oracle fp64 in its precision-model mode -- every contraction
+input rounded to bf16 -- unless a check says "plain"; the GPU run is the
 full-size run):
- * forward rows: out and LSE of sampled query positions (each needs that
-   row's Q and the K/V of every earlier position);
+ * forward rows: out and LSE of sampled query positions drawn uniformly
+   over the whole sequence (each needs that row's Q and the K/V of every
+   earlier position), plus edge rows (first, tile boundaries, last);
  * backward tail: under the causal mask the last T keys are seen only by the
    last T queries, so dQ, dK, dV -- and hence dx -- of the last T positions
    follow from those T rows alone (plus their O/LSE rows);
- * one head's columns of dWo (needs that head's O for every row).
-Everything else at these sizes is pinned by bit-exactness against U = H and
-by the small-size full parity tests.
+ * one head's columns of dWo (needs that head's O for every row);
+ * one KV group's rows of dWqkv (its query heads, its K and V rows: needs
+   the group's whole attention backward, O(L^2 d) per head).
+Everything else at these sizes is pinned by bit-exactness against another
+chunk size and by the small-size full parity tests.
 """
 
 import math
@@ -23,11 +26,12 @@ import torch
 from headwise_chunked_context_gb300 import synth, upipe
 from oracle import upipe_oracle as orc
 from tests.gpu_common import ensure_lib, f64, status_ok
-from tests.tolerance import assert_close, assert_max_abs
+from tests.tolerance import assert_close, assert_close_plain, assert_max_abs
 
 pytestmark = pytest.mark.gpu
 
 D_HEAD = 128
+NAMES = ("out", "lse", "dx", "dWqkv", "dWo")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -68,21 +72,77 @@ def _kv_all(x, W, shape, upto, block=16384):
     return K, V
 
 
-def _run_layer(shape, U, inputs):
+def _nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts)
+
+
+def _run_layer(shape, U, inputs, on_device=None, peaks=None):
+    """Full-size forward + backward.  Returns the five results on the host,
+    or on the device when `on_device` (then the device inputs too).  With a
+    dict `peaks`, records the device high-water mark of each pass's
+    intermediate memory (the helpers size and allocate the workspace; the
+    caller-visible outputs are subtracted)."""
     x, w, wo, dout = inputs
     cfg = upipe.Config(L=shape.L, D=shape.D, H=shape.H, Hkv=shape.Hkv, U=U, rope_theta=shape.theta)
-    xd, wd, wod, dd = (t.to("cuda:0") for t in inputs)
+    dev_in = on_device if on_device is not None else tuple(t.to("cuda:0") for t in inputs)
+    xd, wd, wod, dd = dev_in
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
     out, lse, _ = upipe.layer_forward(cfg, xd, wd, wod)
+    torch.cuda.synchronize()
+    fwd_peak = torch.cuda.max_memory_allocated() - base - _nbytes(out, lse)
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
     dx, dwqkv, dwo = upipe.layer_backward(cfg, xd, wd, wod, dd, lse)
     torch.cuda.synchronize()
+    bwd_peak = torch.cuda.max_memory_allocated() - base - _nbytes(dx, dwqkv, dwo)
     status_ok()
-    res = tuple(t.cpu() for t in (out, lse, dx, dwqkv, dwo))
-    del xd, wd, wod, dd, out, lse, dx, dwqkv, dwo
+    if peaks is not None:
+        peaks[U] = (fwd_peak, bwd_peak)
+    res = (out, lse, dx, dwqkv, dwo)
+    if on_device is not None:
+        return res
+    res = tuple(t.cpu() for t in res)
+    del xd, wd, wod, dd, dev_in, out, lse, dx, dwqkv, dwo
     torch.cuda.empty_cache()
     return res
 
 
-def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None):
+def _fwd_rows(Q, K, V, rows, g, scale, bf):
+    H = Q.shape[1]
+    O = np.empty((len(rows), H, D_HEAD))
+    Lr = np.empty((H, len(rows)))
+    for h in range(H):
+        O[:, h], Lr[h] = orc.attention_head_rows(Q[:, h], rows, K[:, h // g], V[:, h // g], scale, bf16_operands=bf)
+    return O, Lr
+
+
+def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
+    """dQ, dK, dV of the last T positions (RoPE undone on dQ, dK)."""
+    T, H = Qt.shape[0], Qt.shape[1]
+    Hkv = K.shape[1]
+    rnd = orc.bf16_round if bf else (lambda a: a)
+    dq = np.empty((T, H, D_HEAD))
+    dk = np.zeros((T, Hkv, D_HEAD))
+    dv = np.zeros((T, Hkv, D_HEAD))
+    for h in range(H):
+        kh, vh = K[:, h // g], V[:, h // g]
+        o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, bf16_operands=bf)
+        o_t = rnd(o_t)
+        dq[:, h] = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
+        a, b = orc.attention_dkv_tail(Qt[:, h], kh[tpos], vh[tpos], dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
+        dk[:, h // g] += a
+        dv[:, h // g] += b
+    dq = orc.rope_apply(dq, tpos, theta, inverse=True)
+    dk = orc.rope_apply(dk, tpos, theta, inverse=True)
+    return np.concatenate([dq.reshape(T, -1), dk.reshape(T, -1), dv.reshape(T, -1)], 1)
+
+
+def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=False):
+    """Sampled forward rows, the backward tail and one head's dWo columns
+    against the precision-model oracle (and, with `plain`, against the plain
+    fp64 definition as well)."""
     x, w, wo, dout = inputs
     out, lse, dx, dwqkv, dwo = res
     H, Hkv, L = shape.H, shape.Hkv, shape.L
@@ -91,45 +151,40 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None):
     wq_rows = np.arange(H * D_HEAD)
     uni, edge = fwd_rows
     fwd_rows = np.unique(np.concatenate([uni, edge]))
-    need = L if tail else int(fwd_rows.max()) + 1
+    need = L if (tail or dwo_head is not None) else int(fwd_rows.max()) + 1
     K, V = _kv_all(x, w, shape, need)
-    K, V = orc.bf16_round(K), orc.bf16_round(V)
+    Kb, Vb = orc.bf16_round(K), orc.bf16_round(V)
     Wo = wo.to(torch.float64).numpy()
-
-    # forward rows
-    Qr = orc.bf16_round(_proj_rows(x, w, wq_rows, fwd_rows, shape.theta, True))
-    Or = np.empty((len(fwd_rows), H, D_HEAD))
-    Lr = np.empty((H, len(fwd_rows)))
-    for h in range(H):
-        Or[:, h], Lr[h] = orc.attention_head_rows(Qr[:, h], fwd_rows, K[:, h // g], V[:, h // g], scale)
-    ref_out = orc.bf16_round(Or).reshape(len(fwd_rows), -1) @ Wo.T
+    W = w.to(torch.float64).numpy()
     iu = np.searchsorted(fwd_rows, uni)
     ie = np.searchsorted(fwd_rows, edge)
-    assert_close(f64(out[uni]), ref_out[iu], "out rows")
-    assert_close(f64(lse[:, uni]), Lr[:, iu], "lse rows")
+
+    # forward rows
+    Q = _proj_rows(x, w, wq_rows, fwd_rows, shape.theta, True)
+    Or, Lr = _fwd_rows(orc.bf16_round(Q), Kb, Vb, fwd_rows, g, scale, True)
+    ref_out = orc.bf16_round(Or).reshape(len(fwd_rows), -1) @ Wo.T
+    got_out, got_lse = f64(out[uni]), f64(lse[:, uni])
+    assert_close(got_out, ref_out[iu], "out rows")
+    assert_close(got_lse, Lr[:, iu], "lse rows")
     assert_max_abs(f64(out[edge]), ref_out[ie], "out edge rows")
     assert_max_abs(f64(lse[:, edge]), Lr[:, ie], "lse edge rows")
+    if plain:
+        Op, Lp = _fwd_rows(Q, K, V, fwd_rows, g, scale, False)
+        plain_out = Op.reshape(len(fwd_rows), -1) @ Wo.T
+        assert_close_plain(got_out, plain_out[iu], ref_out[iu], "out rows")
+        assert_close_plain(got_lse, Lp[:, iu], Lr[:, iu], "lse rows")
 
     if tail:
         T = tail
         tpos = np.arange(L - T, L)
-        Qt = orc.bf16_round(_proj_rows(x, w, wq_rows, tpos, shape.theta, True))
-        dOt = orc.bf16_round((dout[tpos].to(torch.float64).numpy() @ Wo).reshape(T, H, D_HEAD))
-        dq = np.empty((T, H, D_HEAD))
-        dk = np.zeros((T, Hkv, D_HEAD))
-        dv = np.zeros((T, Hkv, D_HEAD))
-        for h in range(H):
-            kh, vh = K[:, h // g], V[:, h // g]
-            o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale)
-            o_t = orc.bf16_round(o_t)
-            dq[:, h] = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale)
-            a, b = orc.attention_dkv_tail(Qt[:, h], kh[tpos], vh[tpos], dOt[:, h], o_t, l_t, scale)
-            dk[:, h // g] += a
-            dv[:, h // g] += b
-        dq = orc.rope_apply(dq, tpos, shape.theta, inverse=True)
-        dk = orc.rope_apply(dk, tpos, shape.theta, inverse=True)
-        dqkv = np.concatenate([dq.reshape(T, -1), dk.reshape(T, -1), dv.reshape(T, -1)], 1)
-        assert_close(f64(dx[tpos]), dqkv @ w.to(torch.float64).numpy(), "dx tail rows")
+        Qt = _proj_rows(x, w, wq_rows, tpos, shape.theta, True)
+        dOt = (dout[tpos].to(torch.float64).numpy() @ Wo).reshape(T, H, D_HEAD)
+        dqkv = _tail(orc.bf16_round(Qt), orc.bf16_round(dOt), Kb, Vb, tpos, g, scale, True, shape.theta)
+        got = f64(dx[tpos])
+        assert_close(got, dqkv @ W, "dx tail rows")
+        if plain:
+            dqkv_p = _tail(Qt, dOt, K, V, tpos, g, scale, False, shape.theta)
+            assert_close_plain(got, dqkv_p @ W, dqkv @ W, "dx tail rows")
 
     if dwo_head is not None:
         h = dwo_head
@@ -138,34 +193,96 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None):
         for s0 in range(0, L, 16384):
             pos = allpos[s0:s0 + 16384]
             Qh[pos] = _proj_rows(x, w, np.arange(h * D_HEAD, (h + 1) * D_HEAD), pos, shape.theta, True)[:, 0]
-        Oh, _ = orc.attention_head_rows(orc.bf16_round(Qh), allpos, K[:, h // g], V[:, h // g], scale)
-        Oh = orc.bf16_round(Oh)
-        ref = dout.to(torch.float64).numpy().T @ Oh
+        Oh, _ = orc.attention_head_rows(orc.bf16_round(Qh), allpos, Kb[:, h // g], Vb[:, h // g], scale,
+                                        bf16_operands=True)
+        ref = dout.to(torch.float64).numpy().T @ orc.bf16_round(Oh)
         assert_close(f64(dwo[:, h * D_HEAD:(h + 1) * D_HEAD]), ref, "dWo head columns", weight_grad=True)
+    return K, V
+
+
+def _check_dwqkv_group(shape, inputs, dwqkv, kv, K, V):
+    """dWqkv rows of KV group `kv` -- its g query heads' rows, its K rows and
+    its V rows -- from the group's whole attention backward (oracle in its
+    precision-model mode)."""
+    x, w, wo, dout = inputs
+    H, Hkv, L = shape.H, shape.Hkv, shape.L
+    g = H // Hkv
+    heads = np.arange(kv * g, (kv + 1) * g)
+    allpos = np.arange(L)
+    q_rows = np.concatenate([np.arange(h * D_HEAD, (h + 1) * D_HEAD) for h in heads])
+    Q = np.empty((L, g, D_HEAD))
+    for s0 in range(0, L, 16384):
+        pos = allpos[s0:s0 + 16384]
+        Q[pos] = _proj_rows(x, w, q_rows, pos, shape.theta, True)
+    Q = orc.bf16_round(Q)
+    Kj, Vj = orc.bf16_round(K[:, kv:kv + 1]), orc.bf16_round(V[:, kv:kv + 1])
+    O, lse = orc.attention_core_fwd(Q, Kj, Vj, bf16_operands=True)
+    O = orc.bf16_round(O)
+    Wo = wo.to(torch.float64).numpy()
+    cols = np.concatenate([np.arange(h * D_HEAD, (h + 1) * D_HEAD) for h in heads])
+    dO = orc.bf16_round((dout.to(torch.float64).numpy() @ Wo[:, cols]).reshape(L, g, D_HEAD))
+    dq, dk, dv = orc.attention_core_bwd(Q, Kj, Vj, O, lse, dO, bf16_operands=True)
+    dq = orc.rope_apply(dq, allpos, shape.theta, inverse=True)
+    dk = orc.rope_apply(dk, allpos, shape.theta, inverse=True)
+    X = x.to(torch.float64).numpy()
+    ref_q = dq.reshape(L, -1).T @ X
+    ref_k = dk.reshape(L, -1).T @ X
+    ref_v = dv.reshape(L, -1).T @ X
+    got = f64(dwqkv)
+    assert_close(got[q_rows], ref_q, f"dWqkv rows of q heads {heads[0]}..{heads[-1]}", weight_grad=True)
+    rk = slice((H + kv) * D_HEAD, (H + kv + 1) * D_HEAD)
+    rv = slice((H + Hkv + kv) * D_HEAD, (H + Hkv + kv + 1) * D_HEAD)
+    assert_close(got[rk], ref_k, f"dWqkv rows of k head {kv}", weight_grad=True)
+    assert_close(got[rv], ref_v, f"dWqkv rows of v head {kv}", weight_grad=True)
 
 
 def _assert_bit_exact(a, b, what):
-    for x, y, n in zip(a, b, ("out", "lse", "dx", "dWqkv", "dWo")):
+    for x, y, n in zip(a, b, NAMES):
         assert torch.equal(x, y), f"{what}: {n} differs"
 
 
 def test_llama3_8b_layer_L32768():
-    """D=4096, H=32, Hkv=8, U=8 (the benchmark workload), and U=32 bit-exact."""
+    """D=4096, H=32, Hkv=8, U=8 (Llama-3-8B layer shape): oracle rows, tail,
+    dWo columns and one KV group's dWqkv rows, plain-definition figures;
+    U=32 bit-exact."""
     shape = synth.LLAMA8B
     inputs = synth.layer_inputs(shape)
     res = _run_layer(shape, 8, inputs)
-    _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5)
+    K, V = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
+    _check_dwqkv_group(shape, inputs, res[3], 1, K, V)
     _assert_bit_exact(res, _run_layer(shape, 32, inputs), "U=8 vs U=32")
 
 
 def test_qwen32b_shape_layer_L131072_u_sweep():
-    """D=5120, H=64, Hkv=8, U in {64, 16, 8}: identical bits, oracle rows."""
+    """D=5120, H=64, Hkv=8, U in {64, 16, 8}: identical bits, oracle rows,
+    and the measured intermediate memory of each U against the library's
+    arithmetic: chunk bytes scale as U/H, so U=8 keeps 12.5% of the
+    unchunked chunk buffers (the abstract's 87.5% reduction for 32B
+    models)."""
     shape = synth.LayerShape(L=131072, D=5120, H=64, Hkv=8, U=8)
     inputs = synth.layer_inputs(shape)
-    res8 = _run_layer(shape, 8, inputs)
+    peaks = {}
+    res8 = _run_layer(shape, 8, inputs, peaks=peaks)
     _check_layer_rows(shape, inputs, res8, _rows(shape.L, n=6), tail=128)
     for U in (16, 64):
-        _assert_bit_exact(res8, _run_layer(shape, U, inputs), f"U=8 vs U={U}")
+        _assert_bit_exact(res8, _run_layer(shape, U, inputs, peaks=peaks), f"U=8 vs U={U}")
+    chunk = {}
+    for U, (fwd, bwd) in sorted(peaks.items()):
+        cfg = upipe.Config(L=shape.L, D=shape.D, H=shape.H, Hkv=shape.Hkv, U=U)
+        ws_f, ws_b = upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1)
+        cb, fb = upipe.activation_bytes(cfg, 1)
+        chunk[U] = cb
+        print(f"[memory] U={U}: measured fwd {fwd} B (library {ws_f}), bwd {bwd} B (library {ws_b}); "
+              f"bwd chunk {cb} B + fixed {fb} B")
+        # the device high-water mark is the library's workspace (torch's
+        # allocator rounds a large block up to a multiple of 2 MiB)
+        assert ws_f <= fwd <= ws_f + (2 << 20)
+        assert ws_b <= bwd <= ws_b + (2 << 20)
+    for U in (8, 16):
+        assert chunk[U] * 64 == chunk[64] * U
+    print(f"[memory] U=8 chunk buffers: {chunk[8] / chunk[64]:.3f} of U=64 "
+          f"({1 - chunk[8] / chunk[64]:.1%} less)")
+    assert 1 - chunk[8] / chunk[64] == pytest.approx(0.875, abs=0)
 
 
 @pytest.mark.parametrize("L", [65536, 262144])
@@ -178,18 +295,36 @@ def test_long_context_sweep_layer(L):
     _assert_bit_exact(res, _run_layer(shape, 8, inputs), "U=4 vs U=8")
 
 
-def test_long_context_sweep_layer_L1M_early_rows():
-    """L = 1,048,576, U=4: the full-size run; oracle rows in the first 32K
-    positions (a row needs every earlier K/V), finite outputs everywhere."""
-    shape = synth.LayerShape(L=1 << 20, D=4096, H=32, Hkv=8, U=4)
+def _long_layer(L, n_rows):
+    """Llama-3-8B shape, U=4, at L >= 1M: the U=4 and U=8 runs compared bit
+    for bit on the device, then oracle rows drawn over the whole sequence and
+    the last-128 tail of dx."""
+    shape = synth.LayerShape(L=L, D=4096, H=32, Hkv=8, U=4)
     inputs = synth.layer_inputs(shape)
-    res = _run_layer(shape, 4, inputs)
+    dev_in = tuple(t.to("cuda:0") for t in inputs)
+    res4 = _run_layer(shape, 4, inputs, on_device=dev_in)
+    res8 = _run_layer(shape, 8, inputs, on_device=dev_in)
+    _assert_bit_exact(res4, res8, "U=4 vs U=8")
+    del res8, dev_in
+    res = tuple(t.cpu() for t in res4)
+    del res4
+    torch.cuda.empty_cache()
     for t in res:
         assert torch.isfinite(t.float()).all()
-    rng = np.random.default_rng(1)
-    uni = np.unique(rng.integers(0, 32768, 12)).astype(np.int64)
-    edge = np.array([0, 1, 127, 128, 4095, 4096, 32767], dtype=np.int64)
-    _check_layer_rows(shape, inputs, res, (uni, edge), tail=0)
+    _check_layer_rows(shape, inputs, res, _rows(L, n=n_rows, seed=L), tail=128)
+
+
+def test_long_context_sweep_layer_L1M():
+    """L = 1,048,576, U=4: rows over the whole sequence, tail, U=8 bit-exact."""
+    _long_layer(1 << 20, 8)
+
+
+def test_long_context_sweep_layer_L2M():
+    """L = 2,097,152, U=4 (the long-context sweep's largest length; the
+    unchunked U=32 run does not fit: its workspace alone is ~128 GiB on top
+    of the ~96 GiB of layer tensors and fp32 carry): rows over the whole
+    sequence, tail, U=8 bit-exact."""
+    _long_layer(1 << 21, 6)
 
 
 def test_ulysses_slice_core_L1M():
@@ -224,19 +359,20 @@ def test_ulysses_slice_core_L1M():
         rdq = np.empty((len(rows), H, D_HEAD))
         for h in range(H):
             qr = q[rows, h].to(torch.float64).numpy()
-            ro[:, h], rl[h] = orc.attention_head_rows(qr, rows, K, V, scale)
+            ro[:, h], rl[h] = orc.attention_head_rows(qr, rows, K, V, scale, bf16_operands=True)
             ob = orc.bf16_round(ro[:, h])  # o enters the backward as a bf16 tensor
             dor = do[rows, h].to(torch.float64).numpy()
-            rdq[:, h] = orc.attention_dq_rows(qr, rows, K, V, dor, ob, rl[h], scale)
+            rdq[:, h] = orc.attention_dq_rows(qr, rows, K, V, dor, ob, rl[h], scale, bf16_operands=True)
         check = assert_close if kind == "uniform" else assert_max_abs
         check(f64(o[rows]), ro, f"o {kind} rows")
         check(f64(lse[:, rows]), rl, f"lse {kind} rows")
         check(f64(dq[rows]), rdq, f"dq {kind} rows")
     for h in range(H):
         qt = q[tpos, h].to(torch.float64).numpy()
-        ot, lt = orc.attention_head_rows(qt, tpos, K, V, scale)
+        ot, lt = orc.attention_head_rows(qt, tpos, K, V, scale, bf16_operands=True)
         ot = orc.bf16_round(ot)
-        a, b = orc.attention_dkv_tail(qt, K[tpos], V[tpos], do[tpos, h].to(torch.float64).numpy(), ot, lt, scale)
+        a, b = orc.attention_dkv_tail(qt, K[tpos], V[tpos], do[tpos, h].to(torch.float64).numpy(), ot, lt, scale,
+                                      bf16_operands=True)
         dk_t += a
         dv_t += b
     assert_close(f64(dk[tpos, 0]), dk_t, "dk tail")
