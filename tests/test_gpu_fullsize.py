@@ -58,18 +58,25 @@ def _proj_rows(x, W, rows_w, positions, theta, rope):
     return orc.rope_apply(y, positions, theta) if rope else y
 
 
-def _kv_all(x, W, shape, upto, block=16384):
-    """fp64 K (RoPE'd) and V [upto, Hkv, d] from x[:upto], blockwise."""
+def _kv_all(x, W, shape, upto, block=16384, exact=True):
+    """fp64 K (RoPE'd) and V [upto, Hkv, d] from x[:upto], blockwise: the
+    exact values (or None) and their bf16 roundings (the precision model's
+    stored K and V), each block rounded as it is computed."""
     H, Hkv = shape.H, shape.Hkv
     rk = np.arange(H * D_HEAD, (H + Hkv) * D_HEAD)
     rv = np.arange((H + Hkv) * D_HEAD, (H + 2 * Hkv) * D_HEAD)
-    K = np.empty((upto, Hkv, D_HEAD))
-    V = np.empty((upto, Hkv, D_HEAD))
+    K = np.empty((upto, Hkv, D_HEAD)) if exact else None
+    V = np.empty((upto, Hkv, D_HEAD)) if exact else None
+    Kb = np.empty((upto, Hkv, D_HEAD))
+    Vb = np.empty((upto, Hkv, D_HEAD))
     for s0 in range(0, upto, block):
         pos = np.arange(s0, min(upto, s0 + block))
-        K[pos] = _proj_rows(x, W, rk, pos, shape.theta, True)
-        V[pos] = _proj_rows(x, W, rv, pos, shape.theta, False)
-    return K, V
+        k = _proj_rows(x, W, rk, pos, shape.theta, True)
+        v = _proj_rows(x, W, rv, pos, shape.theta, False)
+        Kb[pos], Vb[pos] = orc.bf16_round(k), orc.bf16_round(v)
+        if exact:
+            K[pos], V[pos] = k, v
+    return K, V, Kb, Vb
 
 
 def _nbytes(*ts):
@@ -152,8 +159,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
     uni, edge = fwd_rows
     fwd_rows = np.unique(np.concatenate([uni, edge]))
     need = L if (tail or dwo_head is not None) else int(fwd_rows.max()) + 1
-    K, V = _kv_all(x, w, shape, need)
-    Kb, Vb = orc.bf16_round(K), orc.bf16_round(V)
+    K, V, Kb, Vb = _kv_all(x, w, shape, need, exact=plain)
     Wo = wo.to(torch.float64).numpy()
     W = w.to(torch.float64).numpy()
     iu = np.searchsorted(fwd_rows, uni)
@@ -197,13 +203,13 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
                                         bf16_operands=True)
         ref = dout.to(torch.float64).numpy().T @ orc.bf16_round(Oh)
         assert_close(f64(dwo[:, h * D_HEAD:(h + 1) * D_HEAD]), ref, "dWo head columns", weight_grad=True)
-    return K, V
+    return Kb, Vb
 
 
-def _check_dwqkv_group(shape, inputs, dwqkv, kv, K, V):
+def _check_dwqkv_group(shape, inputs, dwqkv, kv, Kb, Vb):
     """dWqkv rows of KV group `kv` -- its g query heads' rows, its K rows and
     its V rows -- from the group's whole attention backward (oracle in its
-    precision-model mode)."""
+    precision-model mode; Kb, Vb are the stored bf16 K and V)."""
     x, w, wo, dout = inputs
     H, Hkv, L = shape.H, shape.Hkv, shape.L
     g = H // Hkv
@@ -215,7 +221,7 @@ def _check_dwqkv_group(shape, inputs, dwqkv, kv, K, V):
         pos = allpos[s0:s0 + 16384]
         Q[pos] = _proj_rows(x, w, q_rows, pos, shape.theta, True)
     Q = orc.bf16_round(Q)
-    Kj, Vj = orc.bf16_round(K[:, kv:kv + 1]), orc.bf16_round(V[:, kv:kv + 1])
+    Kj, Vj = Kb[:, kv:kv + 1], Vb[:, kv:kv + 1]
     O, lse = orc.attention_core_fwd(Q, Kj, Vj, bf16_operands=True)
     O = orc.bf16_round(O)
     Wo = wo.to(torch.float64).numpy()
@@ -248,8 +254,8 @@ def test_llama3_8b_layer_L32768():
     shape = synth.LLAMA8B
     inputs = synth.layer_inputs(shape)
     res = _run_layer(shape, 8, inputs)
-    K, V = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
-    _check_dwqkv_group(shape, inputs, res[3], 1, K, V)
+    Kb, Vb = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
+    _check_dwqkv_group(shape, inputs, res[3], 1, Kb, Vb)
     _assert_bit_exact(res, _run_layer(shape, 32, inputs), "U=8 vs U=32")
 
 

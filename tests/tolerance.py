@@ -17,9 +17,12 @@ The relative L2 bound applies unchanged to every output.
 
 Against the plain fp64 definition (no rounding anywhere) an implementation
 also carries the precision model's own deviation.  ``assert_close_plain``
-bounds that comparison by the stated rel-L2 and, for max-abs, by the triangle
-inequality: |got - exact| <= |got - model| + |model - exact|, i.e. the
-model's own deviation from the exact result plus the tolerance above.
+bounds that comparison by the triangle inequality, |got - exact| <=
+|got - model| + |model - exact|: each figure (scaled max-abs and rel-L2) is
+at most the model's own deviation from the exact result plus the tolerance
+above.  (At long sequences the bf16 rounding of Q and K alone moves the
+model's late rows by several 1e-3 relative, so the stated rel-L2 cannot
+hold against the exact result there by itself.)
 """
 
 import numpy as np
@@ -73,7 +76,12 @@ def assert_close_plain(got, exact, model, name, weight_grad=False):
     assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{name}: non-finite values"
     max_abs, scaled, rel = report(name, got, exact, weight_grad, against="plain fp64")
     inherent = scaled_max_abs(model, exact, weight_grad)
-    assert rel <= REL_L2, f"{name}: rel-L2 against the plain definition {rel:.3e} > {REL_L2}"
+    _, rel_inherent, _ = errors(model, exact)
+    print(f"[parity] {name}: the precision model itself vs plain fp64: scaled max-abs {inherent:.3e}, "
+          f"rel-L2 {rel_inherent:.3e}")
+    assert rel <= rel_inherent + REL_L2, (
+        f"{name}: rel-L2 against the plain definition {rel:.3e} > the precision model's own "
+        f"{rel_inherent:.3e} + {REL_L2}")
     assert scaled <= inherent + MAX_ABS, (
         f"{name}: scaled max-abs against the plain definition {scaled:.3e} > the precision model's own "
         f"{inherent:.3e} + {MAX_ABS}")
