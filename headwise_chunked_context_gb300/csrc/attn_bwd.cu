@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(dq::kThreadsDq, 1)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int b = j & 1;
-      if (!(ok = warp_wait(bar(B_S_FULL + b), (j >> 1) & 1, w))) break;
-      if (!(ok = warp_wait(bar(B_DP_FULL), j & 1, w))) break;
+      if (!(ok = warp_wait<false, true>(bar(B_S_FULL + b), (j >> 1) & 1, w))) break;
+      if (!(ok = warp_wait<false, true>(bar(B_DP_FULL), j & 1, w))) break;
       tc_fence_after();
       const uint32_t ts = trow + TM_S + b * 128 + half * 64;
       uint32_t s0[32], s1[32], d0[32], d1[32];
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(dq::kThreadsDq, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS_FULL + b));
     }
-    if (ok) ok = warp_wait(bar(B_DQ_DONE), 0, w);
+    if (ok) ok = warp_wait<false, true>(bar(B_DQ_DONE), 0, w);
     if (ok) {
       // Epilogue: this warp writes RoPE pairs (i, i + 64), i in [32 half, 32 half + 32).
       tc_fence_after();
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       // ---- phase 1: P^T over the S^T columns, 16 at a time; the packed
       // P^T of columns 16 h .. 16 h + 15 goes to columns 8 h .. 8 h + 7, which
       // this warp has already read.
-      if (!(ok = warp_wait(bar(B_S_FULL + (grp >> 1)), it & 1, w))) break;
+      if (!(ok = warp_wait<false, true>(bar(B_S_FULL + (grp >> 1)), it & 1, w))) break;
       tc_fence_after();
       float pf[32];
 #pragma unroll
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL + (grp >> 1)));
       // ---- phase 2: dS^T = P^T * (dP^T - Delta) over the dP^T columns
-      if (!(ok = warp_wait(bar(B_DP_FULL), it & 1, w))) break;
+      if (!(ok = warp_wait<false, true>(bar(B_DP_FULL), it & 1, w))) break;
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(dkv::kThreadsKv, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DS_FULL));
     }
-    if (ok) ok = warp_wait(bar(B_DKV_DONE), 0, w);
+    if (ok) ok = warp_wait<false, true>(bar(B_DKV_DONE), 0, w);
     if (ok) {
       tc_fence_after();
       if (p.carry_out) {

@@ -37,9 +37,10 @@
 // tiles (96 for D = 4096, U = 8 query and 2 KV heads: 1.26 waves of 76
 // pairs), so it splits K at k_mid into two work units per tile, each reduced
 // (red.global.add.f32) into the zeroed output: 192 units fill the pairs 2.5
-// times instead of 1.26.  Two addends into a zero give the same bits in
-// either order, and k_mid depends only on L, so the result stays
-// deterministic and independent of U.
+// times instead of 1.26.  dWo does the same (80 pair tiles at D = 5120,
+// U = 8: a second wave of 4 tiles unsplit).  Two addends into a zero give
+// the same bits in either order, and k_mid depends only on L, so the result
+// stays deterministic and independent of U.
 //
 // The carried fp32 partials (out32, dx32) move between global memory and the
 // epilogue warps through a swizzled shared staging tile per warp: TMEM gives
@@ -305,7 +306,7 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
     } else {  // GK_DWQKV
       frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
     }
-    const bool reduce = KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks;
+    const bool reduce = (KIND == GK_DWQKV || KIND == GK_DWO) && p.k_mid > 0 && p.k_mid < p.k_blocks;
     if constexpr (kCarry) {
       if (!p.final_out) {
         const int m0 = m - (r & 31);
@@ -371,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n_pairs = (p.n_tiles + 1) / 2;
   const int tiles = m_pairs * n_pairs;
   // Work unit t: pair tile t % tiles over K blocks [kb_lo(t), kb_hi(t)).
-  const bool ksplit = KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks;
+  const bool ksplit = (KIND == GK_DWQKV || KIND == GK_DWO) && p.k_mid > 0 && p.k_mid < p.k_blocks;
   const int total = ksplit ? 2 * tiles : tiles;
   auto kb_lo = [&](int t) { return ksplit && t >= tiles ? p.k_mid : 0; };
   auto kb_hi = [&](int t) { return ksplit && t < tiles ? p.k_mid : p.k_blocks; };
@@ -602,7 +603,7 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
     resident[dev] = n > 0 ? n : 1;
   }
   const int tiles = ((p.m_tiles + 1) / 2) * ((p.n_tiles + 1) / 2);
-  const int total = (KIND == GK_DWQKV && p.k_mid > 0 && p.k_mid < p.k_blocks) ? 2 * tiles : tiles;
+  const int total = ((KIND == GK_DWQKV || KIND == GK_DWO) && p.k_mid > 0 && p.k_mid < p.k_blocks) ? 2 * tiles : tiles;
   const int pairs = total < resident[dev] ? total : resident[dev];
   if (pairs <= 0) return cudaSuccess;
   gemm_kernel<KIND><<<2 * pairs, kThreads, smem, s>>>(a, b, p);

@@ -179,15 +179,22 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // ago, against about 15 for one warp-wide probe.  The abort flag and the
 // clock are checked every 32 rounds, by warp vote.  Must be called by all 32
 // lanes; the result is warp-uniform.
-template <bool kCluster = false>
+//
+// kSuspend probes with try_wait, which suspends the warp in hardware until
+// the phase completes (or a system time limit passes) instead of spinning:
+// for warps that wait long and often (the backward kernels' compute warps),
+// spinning probes took a third of the load/store issue slots and competed
+// for issue slots with the MMA-issuing threads on the same sub-partitions.
+template <bool kCluster = false, bool kSuspend = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (__all_sync(0xffffffffu, mbar_test<kCluster>(bar, parity))) return true;
-    if ((i & 31) != 0) continue;
+    const bool done = kSuspend ? mbar_try_wait<kCluster>(bar, parity) : mbar_test<kCluster>(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if (!kSuspend && (i & 31) != 0) continue;
     if (__any_sync(0xffffffffu, *w.abort_flag != 0)) return false;
     const uint64_t now = sm_cycles();
-    if (i == 32) {
+    if (i == (kSuspend ? 1u : 32u)) {
       t0 = now;
     } else if (__any_sync(0xffffffffu, now - t0 > w.limit_ns * kCyclesPerNs)) {
       if ((threadIdx.x & 31) == 0) {

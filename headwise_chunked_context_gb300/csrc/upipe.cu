@@ -599,6 +599,15 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     dw.out_col0 = ch.q0 * 128;
     dw.out = dWo;
     dw.ld_out = Hd;
+    // K (tokens) in two halves reduced into the zeroed columns, split where
+    // dWqkv splits (depends on L alone).
+    dw.k_mid = dw.k_blocks >= 2 && dw.m_tiles <= kMaxSlots ? (dw.k_blocks + 1) / 2 : 0;
+    if (dw.k_mid > 0) {
+      int16_t rows[kMaxSlots];
+      for (int b = 0; b < dw.m_tiles; ++b) rows[b] = static_cast<int16_t>(b);
+      UPIPE_LAUNCH(UPIPE_KIND_ZERO_ROWS,
+                   launch_zero_rows(dWo + dw.out_col0, Hd, dw.N, rows, dw.m_tiles, st));
+    }
     UPIPE_LAUNCH(UPIPE_KIND_DWO_GEMM, launch_gemm(GK_DWO, m_dout_mn, m_o_mn, dw, st));
 
     // Attention backward (a-5): dQ, then dK/dV (carried when U < g).

@@ -49,10 +49,17 @@ says -- while every product, sum and element-wise step stays exact fp64
 
 * stored tensors that feed the next contraction: Q and K after RoPE, V, the
   attention output O, and dO = dout Wo;
-* the softmax tiles where they enter a product: the probabilities
-  P = exp(S - LSE) in P V (forward) and in P^T dO (backward), and
-  dS = P * (dP - Delta) in dS K and dS^T Q.  P inside dS's element-wise
-  formula is not a contraction input and stays exact.
+* the softmax tiles of the backward where they enter a product: the
+  probabilities P = exp(S - LSE) in P^T dO and in the recomputation of
+  O = P V from the forward's LSE, and dS = P * (dP - Delta) in dS K and
+  dS^T Q.  P inside dS's element-wise formula is not a contraction input and
+  stays exact.
+
+The forward output's own P V (``layer_fwd``) keeps P exact: an online
+softmax rounds exp(S - running maximum), a quantity the definition does not
+fix, so its rounding is left to the implementation's tolerance.  The
+backward recomputes O "from LSE", where P = exp(S - LSE) is the definition's
+own quantity (``p_bf16`` of the forward helpers selects this).
 
 This isolates an implementation's own arithmetic (accumulation order, fp32
 element-wise math) from the rounding the precision model itself implies.
@@ -155,12 +162,13 @@ def _op(a, bf16_operands):
     return bf16_round(a) if bf16_operands else a
 
 
-def attention_head_rows(qr, qpos, k, v, scale, bf16_operands=False):
+def attention_head_rows(qr, qpos, k, v, scale, p_bf16=False):
     """O rows and LSE for query rows ``qr`` [n, d] at positions ``qpos``.
 
     ``k``, ``v`` [Lk, d] are this head's keys/values (KV head h // g).
-    Key j is visible to the query at position p iff j <= p.  With
-    ``bf16_operands`` the probabilities exp(S - LSE) enter P V as bf16.
+    Key j is visible to the query at position p iff j <= p.  With ``p_bf16``
+    the probabilities exp(S - LSE) enter P V as bf16 (O recomputed from the
+    LSE, module header).
     """
     qr = np.asarray(qr, dtype=F64)
     qpos = np.asarray(qpos)
@@ -178,12 +186,13 @@ def attention_head_rows(qr, qpos, k, v, scale, bf16_operands=False):
         l = np.exp(S - m[:, None]).sum(axis=1)
         lse[s0:s1] = m + np.log(l)
         P = np.exp(S - lse[s0:s1, None])
-        o[s0:s1] = _op(P, bf16_operands) @ v[:top]
+        o[s0:s1] = _op(P, p_bf16) @ v[:top]
     return o, lse
 
 
-def attention_core_fwd(q, k, v, causal=True, bf16_operands=False):
-    """O [L, H, d] and LSE [H, L] for q [L, H, d], k/v [L, Hkv, d]."""
+def attention_core_fwd(q, k, v, causal=True, p_bf16=False):
+    """O [L, H, d] and LSE [H, L] for q [L, H, d], k/v [L, Hkv, d]; with
+    ``p_bf16`` P enters P V as bf16 (see attention_head_rows)."""
     assert causal, "only the causal square mask is defined here"
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -196,7 +205,7 @@ def attention_core_fwd(q, k, v, causal=True, bf16_operands=False):
     lse = np.zeros((H, L), dtype=F64)
     pos = np.arange(L)
     for h in range(H):
-        o[:, h], lse[h] = attention_head_rows(q[:, h], pos, k[:, h // g], v[:, h // g], scale, bf16_operands)
+        o[:, h], lse[h] = attention_head_rows(q[:, h], pos, k[:, h // g], v[:, h // g], scale, p_bf16)
     return o, lse
 
 
@@ -299,7 +308,7 @@ def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None, bf16_operands=False):
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
     q, k, v = _op(q, bf16_operands), _op(k, bf16_operands), _op(v, bf16_operands)
-    o, lse = attention_core_fwd(q, k, v, bf16_operands=bf16_operands)
+    o, lse = attention_core_fwd(q, k, v)  # the forward's own P V: P exact (module header)
     o = _op(o, bf16_operands)
     out = o.reshape(x.shape[0], H * d) @ Wo.T
     return out, lse, o
@@ -321,7 +330,9 @@ def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_operands=False):
         d = Wo.shape[1] // H
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
     q, k, v = _op(q, bf16_operands), _op(k, bf16_operands), _op(v, bf16_operands)
-    o, lse = attention_core_fwd(q, k, v, bf16_operands=bf16_operands)
+    # O recomputed from the forward's LSE (P = exp(S - LSE), bf16 in P V
+    # under the precision model).
+    o, lse = attention_core_fwd(q, k, v, p_bf16=bf16_operands)
     o = _op(o, bf16_operands)
     o_flat = o.reshape(L, H * d)
     dWo = dout.T @ o_flat

@@ -50,7 +50,7 @@ def test_core_fwd_bwd_matches_oracle(L, H, Hkv, U):
     (q, k, v, do), (o, lse, dq, dk, dv) = _core(L, H, Hkv, U)
     q, k, v, do = f64(q), f64(k), f64(v), f64(do)
     got = [f64(t) for t in (o, lse, dq, dk, dv)]
-    ro, rlse = orc.attention_core_fwd(q, k, v, bf16_operands=True)
+    ro, rlse = orc.attention_core_fwd(q, k, v)  # the forward output: P exact
     # o enters the backward as the bf16 tensor the forward returns
     model = (ro, rlse, *orc.attention_core_bwd(q, k, v, orc.bf16_round(ro), rlse, do, bf16_operands=True))
     po, plse = orc.attention_core_fwd(q, k, v)

@@ -116,12 +116,13 @@ def _run_layer(shape, U, inputs, on_device=None, peaks=None):
     return res
 
 
-def _fwd_rows(Q, K, V, rows, g, scale, bf):
+def _fwd_rows(Q, K, V, rows, g, scale):
+    """Forward output rows (the forward's own P V keeps P exact)."""
     H = Q.shape[1]
     O = np.empty((len(rows), H, D_HEAD))
     Lr = np.empty((H, len(rows)))
     for h in range(H):
-        O[:, h], Lr[h] = orc.attention_head_rows(Q[:, h], rows, K[:, h // g], V[:, h // g], scale, bf16_operands=bf)
+        O[:, h], Lr[h] = orc.attention_head_rows(Q[:, h], rows, K[:, h // g], V[:, h // g], scale)
     return O, Lr
 
 
@@ -135,7 +136,8 @@ def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
     dv = np.zeros((T, Hkv, D_HEAD))
     for h in range(H):
         kh, vh = K[:, h // g], V[:, h // g]
-        o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, bf16_operands=bf)
+        # O recomputed from the LSE, as the backward does
+        o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, p_bf16=bf)
         o_t = rnd(o_t)
         dq[:, h] = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
         a, b = orc.attention_dkv_tail(Qt[:, h], kh[tpos], vh[tpos], dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
@@ -167,7 +169,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
 
     # forward rows
     Q = _proj_rows(x, w, wq_rows, fwd_rows, shape.theta, True)
-    Or, Lr = _fwd_rows(orc.bf16_round(Q), Kb, Vb, fwd_rows, g, scale, True)
+    Or, Lr = _fwd_rows(orc.bf16_round(Q), Kb, Vb, fwd_rows, g, scale)
     ref_out = orc.bf16_round(Or).reshape(len(fwd_rows), -1) @ Wo.T
     got_out, got_lse = f64(out[uni]), f64(lse[:, uni])
     assert_close(got_out, ref_out[iu], "out rows")
@@ -175,7 +177,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
     assert_max_abs(f64(out[edge]), ref_out[ie], "out edge rows")
     assert_max_abs(f64(lse[:, edge]), Lr[:, ie], "lse edge rows")
     if plain:
-        Op, Lp = _fwd_rows(Q, K, V, fwd_rows, g, scale, False)
+        Op, Lp = _fwd_rows(Q, K, V, fwd_rows, g, scale)
         plain_out = Op.reshape(len(fwd_rows), -1) @ Wo.T
         assert_close_plain(got_out, plain_out[iu], ref_out[iu], "out rows")
         assert_close_plain(got_lse, Lp[:, iu], Lr[:, iu], "lse rows")
@@ -200,7 +202,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
             pos = allpos[s0:s0 + 16384]
             Qh[pos] = _proj_rows(x, w, np.arange(h * D_HEAD, (h + 1) * D_HEAD), pos, shape.theta, True)[:, 0]
         Oh, _ = orc.attention_head_rows(orc.bf16_round(Qh), allpos, Kb[:, h // g], Vb[:, h // g], scale,
-                                        bf16_operands=True)
+                                        p_bf16=True)  # the backward's O, recomputed from the LSE
         ref = dout.to(torch.float64).numpy().T @ orc.bf16_round(Oh)
         assert_close(f64(dwo[:, h * D_HEAD:(h + 1) * D_HEAD]), ref, "dWo head columns", weight_grad=True)
     return Kb, Vb
@@ -222,7 +224,7 @@ def _check_dwqkv_group(shape, inputs, dwqkv, kv, Kb, Vb):
         Q[pos] = _proj_rows(x, w, q_rows, pos, shape.theta, True)
     Q = orc.bf16_round(Q)
     Kj, Vj = Kb[:, kv:kv + 1], Vb[:, kv:kv + 1]
-    O, lse = orc.attention_core_fwd(Q, Kj, Vj, bf16_operands=True)
+    O, lse = orc.attention_core_fwd(Q, Kj, Vj, p_bf16=True)  # the backward's O, from the LSE
     O = orc.bf16_round(O)
     Wo = wo.to(torch.float64).numpy()
     cols = np.concatenate([np.arange(h * D_HEAD, (h + 1) * D_HEAD) for h in heads])
@@ -365,8 +367,9 @@ def test_ulysses_slice_core_L1M():
         rdq = np.empty((len(rows), H, D_HEAD))
         for h in range(H):
             qr = q[rows, h].to(torch.float64).numpy()
-            ro[:, h], rl[h] = orc.attention_head_rows(qr, rows, K, V, scale, bf16_operands=True)
-            ob = orc.bf16_round(ro[:, h])  # o enters the backward as a bf16 tensor
+            # the core forward's output (P exact); o enters the backward as a bf16 tensor
+            ro[:, h], rl[h] = orc.attention_head_rows(qr, rows, K, V, scale)
+            ob = orc.bf16_round(ro[:, h])
             dor = do[rows, h].to(torch.float64).numpy()
             rdq[:, h] = orc.attention_dq_rows(qr, rows, K, V, dor, ob, rl[h], scale, bf16_operands=True)
         check = assert_close if kind == "uniform" else assert_max_abs
@@ -375,7 +378,7 @@ def test_ulysses_slice_core_L1M():
         check(f64(dq[rows]), rdq, f"dq {kind} rows")
     for h in range(H):
         qt = q[tpos, h].to(torch.float64).numpy()
-        ot, lt = orc.attention_head_rows(qt, tpos, K, V, scale, bf16_operands=True)
+        ot, lt = orc.attention_head_rows(qt, tpos, K, V, scale)
         ot = orc.bf16_round(ot)
         a, b = orc.attention_dkv_tail(qt, K[tpos], V[tpos], do[tpos, h].to(torch.float64).numpy(), ot, lt, scale,
                                       bf16_operands=True)

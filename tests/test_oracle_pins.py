@@ -353,10 +353,11 @@ def _bf(a):
 
 def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs():
     """With bf16_operands the layer equals a restatement written here from
-    the definition, whose every contraction input (Q, K, V after RoPE, P in
-    P V and P^T dO, O, dO, dS in dS K and dS^T Q) goes through torch's bf16
-    conversion, with all else exact; and it differs from the exact layer
-    only at the bf16 level."""
+    the definition, whose every contraction input (Q, K, V after RoPE, O,
+    dO; P in the backward's recomputation of O from the LSE and in P^T dO;
+    dS in dS K and dS^T Q) goes through torch's bf16 conversion, with all
+    else exact (the forward output's own P V keeps P exact); and it differs
+    from the exact layer only at the bf16 level."""
     x, Wqkv, Wo, dout, H, Hkv, theta = _micro(seed=3, L=24, D=32)
     L = x.shape[0]
     d = Wo.shape[1] // H
@@ -369,12 +370,15 @@ def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs()
     lse = np.zeros((H, L))
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     causal = np.tril(np.ones((L, L), dtype=bool))
+    o_fwd = np.zeros((L, H, d))
     for h in range(H):
         S = q[:, h] @ k[:, h // g].T * sc
         S[~causal] = -np.inf
         lse[h] = logsumexp(S, axis=1)
         P = np.exp(S - lse[h][:, None])
+        o_fwd[:, h] = P @ v[:, h // g]
         o[:, h] = _bf(P) @ v[:, h // g]
+    o_fwd = _bf(o_fwd)
     o = _bf(o)
     do = _bf((dout @ Wo).reshape(L, H, d))
     for h in range(H):
@@ -386,8 +390,8 @@ def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs()
         dk[:, h // g] += dS.T @ q[:, h] * sc
         dq[:, h] = dS @ k[:, h // g] * sc
     np.testing.assert_allclose(lse_b, lse, atol=1e-13)
-    np.testing.assert_allclose(o_b, o, atol=1e-13)
-    np.testing.assert_allclose(out_b, o.reshape(L, -1) @ Wo.T, atol=1e-13)
+    np.testing.assert_allclose(o_b, o_fwd, atol=1e-13)
+    np.testing.assert_allclose(out_b, o_fwd.reshape(L, -1) @ Wo.T, atol=1e-13)
     pos = np.arange(L)
     dqkv = np.concatenate([orc.rope_apply(dq, pos, theta, inverse=True).reshape(L, -1),
                            orc.rope_apply(dk, pos, theta, inverse=True).reshape(L, -1), dv.reshape(L, -1)], 1)
@@ -463,9 +467,9 @@ def test_multi_block_results_equal_single_block(monkeypatch):
     sc = 1 / math.sqrt(d)
 
     def run(bf):
-        o, lse = orc.attention_core_fwd(q, k, v, bf16_operands=bf)
+        o, lse = orc.attention_core_fwd(q, k, v, p_bf16=bf)
         grads = orc.attention_core_bwd(q, k, v, o, lse, do, bf16_operands=bf)
-        ro, rl = orc.attention_head_rows(q[rows, 1], rows, k[:, 0], v[:, 0], sc, bf16_operands=bf)
+        ro, rl = orc.attention_head_rows(q[rows, 1], rows, k[:, 0], v[:, 0], sc, p_bf16=bf)
         rdq = orc.attention_dq_rows(q[rows, 1], rows, k[:, 0], v[:, 0], do[rows, 1], o[rows, 1], lse[1, rows], sc,
                                     bf16_operands=bf)
         return (o, lse, *grads, ro, rl, rdq)
