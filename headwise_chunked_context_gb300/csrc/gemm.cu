@@ -47,6 +47,8 @@
 // each lane one row, and 16-byte accesses to 32 different rows per warp
 // instruction left the carry stream latency-bound; through the tile, each
 // global access instruction covers four whole 128-byte rows.
+#include <atomic>
+
 #include "sm103_ptx.cuh"
 
 namespace upipe {
@@ -560,15 +562,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// Multiprocessor count of the current device (cached per device).
+// Multiprocessor count of the current device (cached per device; atomic
+// entries, so host threads filling the same entry together are well defined).
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  static int cached[64] = {0};
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  static std::atomic<int> cached[64];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -580,11 +586,11 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
   // Persistent: as many pairs as can be resident at once.  A pair must fit
   // inside one GPC, so that is fewer than SMs / 2 when GPCs have odd SM
   // counts; more pairs than that would run as a second wave.
-  static int resident[64] = {0};
+  static std::atomic<int> resident[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[dev] <= 0) {
+  if (resident[dev].load(std::memory_order_relaxed) <= 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count()), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -600,11 +606,12 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<KIND>, &cfg);
     if (e != cudaSuccess) return e;
-    resident[dev] = n > 0 ? n : 1;
+    resident[dev].store(n > 0 ? n : 1, std::memory_order_relaxed);
   }
+  const int res = resident[dev].load(std::memory_order_relaxed);
   const int tiles = ((p.m_tiles + 1) / 2) * ((p.n_tiles + 1) / 2);
   const int total = ((KIND == GK_DWQKV || KIND == GK_DWO) && p.k_mid > 0 && p.k_mid < p.k_blocks) ? 2 * tiles : tiles;
-  const int pairs = total < resident[dev] ? total : resident[dev];
+  const int pairs = total < res ? total : res;
   if (pairs <= 0) return cudaSuccess;
   gemm_kernel<KIND><<<2 * pairs, kThreads, smem, s>>>(a, b, p);
   return cudaGetLastError();
