@@ -450,7 +450,13 @@ def run_upipe(args, w, world, rank, local):
                  "flops_per_step": attn_f, "frac_of_burst": attn_f / (attn_ms / 1e3) / 1e12 / burst,
                  "note": "7 L^2 H d over the step time less the projection kernels' event time"}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Each step
+    # copies its inputs (x, Wqkv, Wo, dout) from pinned host memory and its
+    # results (out, LSE, dx, dWqkv, dWo) back.  Two device buffer sets let
+    # step k + 1's host->device copies run on a copy stream while step k
+    # computes, and step k's device->host copies while step k + 1 computes
+    # (a pipelined loader); the timed region opens before the first copy and
+    # closes after the last, so every byte of every step crosses inside it.
     e2e = None
     if rank == 0 or world > 1:
         pin = lambda t: t.to("cpu").pin_memory()
@@ -460,48 +466,94 @@ def run_upipe(args, w, world, rank, local):
         h2d = _bytes(hx, hw, hwo, hd)
         d2h = _bytes(ho, hl, hdx, hdw, hdwo)
         k_e2e = max(3, min(args.steps, 10))
+        sets = [(x, wqkv, wo, dout, out, lse, dx, dwqkv, dwo),
+                tuple(torch.empty_like(t) for t in (x, wqkv, wo, dout, out, lse, dx, dwqkv, dwo))]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ready = [torch.cuda.Event(), torch.cuda.Event()]    # inputs of buffer set b landed
+        done = [torch.cuda.Event(), torch.cuda.Event()]     # compute on buffer set b finished
+        free = [torch.cuda.Event(), torch.cuda.Event()]     # buffer set b's results copied out
 
-        # Copies that the layer does not wait for run on a second stream:
-        # dout streams in during the forward, out and LSE stream back during
-        # the backward.  Every byte still crosses inside the timed region.
-        cstream = torch.cuda.Stream(dev)
-        ev = [torch.cuda.Event() for _ in range(3)]
+        def load(b):
+            s_in.wait_event(free[b])
+            with torch.cuda.stream(s_in):
+                for dst, src in zip(sets[b][:4], (hx, hw, hwo, hd)):
+                    dst.copy_(src, non_blocking=True)
+                ready[b].record(s_in)
 
-        def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            wqkv.copy_(hw, non_blocking=True)
-            wo.copy_(hwo, non_blocking=True)
-            ev[0].record(stream)
-            cstream.wait_event(ev[0])                 # dout's buffer is free (previous bwd done)
-            with torch.cuda.stream(cstream):
-                dout.copy_(hd, non_blocking=True)
-                ev[1].record(cstream)
-            upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
-            ev[2].record(stream)
-            stream.wait_event(ev[1])                  # dout landed
-            upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream)
-            cstream.wait_event(ev[2])                 # out and LSE final
-            with torch.cuda.stream(cstream):
-                ho.copy_(out, non_blocking=True)
-                hl.copy_(lse, non_blocking=True)
-            hdx.copy_(dx, non_blocking=True)
-            hdw.copy_(dwqkv, non_blocking=True)
-            hdwo.copy_(dwo, non_blocking=True)
-            stream.wait_stream(cstream)               # the step ends when every copy has landed
+        def compute(b):
+            bx, bw, bwo, bd, bo, bl, bdx, bdw, bdwo = sets[b]
+            stream.wait_event(ready[b])
+            upipe.attn_fwd(cfg, bx, bw, bwo, bo, bl, None, ws, stream)
+            upipe.attn_bwd(cfg, bx, bw, bwo, bd, bl, bdx, bdw, bdwo, None, ws, stream)
+            done[b].record(stream)
+            s_out.wait_event(done[b])
+            with torch.cuda.stream(s_out):
+                for dst, src in zip((ho, hl, hdx, hdw, hdwo), (bo, bl, bdx, bdw, bdwo)):
+                    dst.copy_(src, non_blocking=True)
+                free[b].record(s_out)
 
-        e2e_step()
+        def run(n):
+            for b in (0, 1):
+                free[b].record(s_out)
+            load(0)
+            for k in range(n):
+                if k + 1 < n:
+                    load((k + 1) % 2)
+                compute(k % 2)
+            stream.wait_stream(s_out)
+
+        run(2)  # warm-up of the copy path
         torch.cuda.synchronize(dev)
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(k_e2e):
-            e2e_step()
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        run(k_e2e)
         a1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(a0.elapsed_time(a1) / k_e2e, dev)
         e2e = {"value": world * step_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": k_e2e}
-        del hx, hw, hwo, hd, ho, hl, hdx, hdw, hdwo
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": k_e2e,
+               "note": "pinned host buffers; two device buffer sets, host<->device copies on two copy streams "
+                       "overlapping the neighbouring steps' compute; all copies inside the timed region"}
+        del hx, hw, hwo, hd, ho, hl, hdx, hdw, hdwo, sets
+
+    # ---- activation offload: the block input x to pinned host memory and
+    # back on the library's copy streams, alone and beside one layer step.
+    offload = None
+    if rank == 0 or world > 1:
+        hbuf = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hsrc = x.to("cpu").pin_memory()
+        dbuf = torch.empty_like(x)
+        nbytes = _bytes(x)
+
+        def timed_copies(fn):
+            torch.cuda.synchronize(dev)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            fn()
+            upipe.copies_join(stream)
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            return a0.elapsed_time(a1)
+
+        timed_copies(lambda: (upipe.offload_async(hbuf, x, stream), upipe.prefetch_async(dbuf, hsrc, stream)))
+        off_ms = timed_copies(lambda: upipe.offload_async(hbuf, x, stream))
+        pre_ms = timed_copies(lambda: upipe.prefetch_async(dbuf, hsrc, stream))
+        both_ms = timed_copies(lambda: step())
+        with_ms = timed_copies(lambda: (upipe.offload_async(hbuf, x, stream), upipe.prefetch_async(dbuf, hsrc, stream),
+                                        step()))
+        offload = {"bytes": nbytes, "offload_ms": off_ms, "prefetch_ms": pre_ms,
+                   "offload_gbs": nbytes / off_ms / 1e6, "prefetch_gbs": nbytes / pre_ms / 1e6,
+                   "step_ms": both_ms, "step_with_copies_ms": with_ms,
+                   "note": "x of the workload to pinned host memory and back over the host link, timed alone; "
+                           "then one layer step with an x-sized offload and prefetch in flight beside it"}
+        if not torch.equal(dbuf, x) or not torch.equal(hbuf, hsrc):
+            raise RuntimeError("offload/prefetch round trip changed the data")
+        del hbuf, hsrc, dbuf
+        check_status("after the offload measurement")
 
     # ---- peak activation bytes and throughput against U (measured)
     del ws
@@ -539,7 +591,7 @@ def run_upipe(args, w, world, rank, local):
                 "note": "hardware flops: the layer flops plus the backward's recompute of QKV and attention fwd"},
         "roofline": roofline, "kernels": kernels, "profiled_step_ms": prof_step_ms,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks, "u_sweep": sweep,
+        "clocks": clocks, "u_sweep": sweep, "offload": offload,
     }
     print(json.dumps(line), flush=True)
 

@@ -304,6 +304,53 @@ int launch_attn_bwd_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   return UPIPE_OK;
 }
 
+// Copy streams of the activation offload: one per direction and device,
+// created on first use, with an event to order each batch of copies after
+// the caller's stream and one per direction to join them back.
+struct Copier {
+  cudaStream_t d2h = nullptr, h2d = nullptr;
+  cudaEvent_t after = nullptr, done_d2h = nullptr, done_h2d = nullptr;
+};
+Copier g_copier[kMaxDev];
+std::mutex g_copier_mu;
+
+int copier(Copier** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UPIPE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDev) return UPIPE_ERR_UNSUPPORTED_DEVICE;
+  Copier& c = g_copier[dev];
+  if (!c.done_h2d) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return UPIPE_ERR_CUDA;
+    if (!c.d2h && cudaStreamCreateWithPriority(&c.d2h, cudaStreamNonBlocking, least) != cudaSuccess)
+      return UPIPE_ERR_CUDA;
+    if (!c.h2d && cudaStreamCreateWithPriority(&c.h2d, cudaStreamNonBlocking, least) != cudaSuccess)
+      return UPIPE_ERR_CUDA;
+    if (!c.after && cudaEventCreateWithFlags(&c.after, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
+    if (!c.done_d2h && cudaEventCreateWithFlags(&c.done_d2h, cudaEventDisableTiming) != cudaSuccess)
+      return UPIPE_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&c.done_h2d, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
+  }
+  *out = &c;
+  return UPIPE_OK;
+}
+
+// One copy on the direction's copy stream, after the caller's stream.
+int async_copy(void* dst, const void* src, size_t bytes, bool to_host, cudaStream_t st) {
+  if (bytes == 0) return UPIPE_OK;
+  if (!dst || !src) return UPIPE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_copier_mu);
+  Copier* c = nullptr;
+  if (int e = copier(&c)) return e;
+  cudaStream_t cs = to_host ? c->d2h : c->h2d;
+  if (cudaEventRecord(c->after, st) != cudaSuccess || cudaStreamWaitEvent(cs, c->after, 0) != cudaSuccess)
+    return UPIPE_ERR_CUDA;
+  if (cudaMemcpyAsync(dst, src, bytes, to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, cs) !=
+      cudaSuccess)
+    return UPIPE_ERR_CUDA;
+  return UPIPE_OK;
+}
+
 #define UPIPE_MAP(x)                                 \
   do {                                               \
     if (!(x)) return UPIPE_ERR_CUDA;                 \
@@ -804,6 +851,25 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
     b.limit_ns = limit;
     if (int e = launch_attn_bwd_pair(mq, mk, mv, mdo, b, m_tiles, st)) return e;
   }
+  return UPIPE_OK;
+}
+
+int upipe_offload_async(void* host_dst, const void* dev_src, size_t bytes, void* stream) {
+  return async_copy(host_dst, dev_src, bytes, true, static_cast<cudaStream_t>(stream));
+}
+
+int upipe_prefetch_async(void* dev_dst, const void* host_src, size_t bytes, void* stream) {
+  return async_copy(dev_dst, host_src, bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+int upipe_copies_join(void* stream) {
+  std::lock_guard<std::mutex> lock(g_copier_mu);
+  Copier* c = nullptr;
+  if (int e = copier(&c)) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaEventRecord(c->done_d2h, c->d2h) != cudaSuccess || cudaEventRecord(c->done_h2d, c->h2d) != cudaSuccess ||
+      cudaStreamWaitEvent(st, c->done_d2h, 0) != cudaSuccess || cudaStreamWaitEvent(st, c->done_h2d, 0) != cudaSuccess)
+    return UPIPE_ERR_CUDA;
   return UPIPE_OK;
 }
 

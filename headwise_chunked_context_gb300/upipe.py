@@ -36,6 +36,9 @@ EXPORTS = (
     "upipe_attn_core_fwd",
     "upipe_attn_core_bwd",
     "upipe_attn_core_bwd_noalloc",
+    "upipe_offload_async",
+    "upipe_prefetch_async",
+    "upipe_copies_join",
     "upipe_last_device_status",
     "upipe_debug_wait_timeout",
     "upipe_launch_count",
@@ -114,6 +117,12 @@ def lib() -> ctypes.CDLL:
         L.upipe_attn_core_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_core_bwd_noalloc.restype = ctypes.c_int
         L.upipe_attn_core_bwd_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P]
+        L.upipe_offload_async.restype = ctypes.c_int
+        L.upipe_offload_async.argtypes = [P, P, ctypes.c_size_t, P]
+        L.upipe_prefetch_async.restype = ctypes.c_int
+        L.upipe_prefetch_async.argtypes = [P, P, ctypes.c_size_t, P]
+        L.upipe_copies_join.restype = ctypes.c_int
+        L.upipe_copies_join.argtypes = [P]
         L.upipe_last_device_status.restype = ctypes.c_int
         L.upipe_last_device_status.argtypes = [P]
         L.upipe_debug_wait_timeout.restype = ctypes.c_int
@@ -310,6 +319,42 @@ def attn_core_bwd_noalloc(cfg: Config, q, k, v, o, lse, do, dq, dk, dv, stream=N
     _check(lib().upipe_attn_core_bwd_noalloc(ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                              _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
            "upipe_attn_core_bwd_noalloc")
+
+
+def _host_pair(host, devt, name):
+    if host.is_cuda or not devt.is_cuda:
+        raise ValueError(f"{name}: expected a host tensor and a CUDA tensor")
+    if tuple(host.shape) != tuple(devt.shape) or host.dtype != devt.dtype:
+        raise ValueError(f"{name}: host {tuple(host.shape)} {host.dtype} vs device {tuple(devt.shape)} {devt.dtype}")
+    if not host.is_contiguous() or not devt.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous tensors")
+    _on_device(**{name: devt})
+    return devt.numel() * devt.element_size()
+
+
+def offload_async(host, dev_tensor, stream=None) -> None:
+    """Copies `dev_tensor` into the host tensor `host` (pinned for an
+    asynchronous copy) on the library's copy stream, after the work already
+    on `stream` (upipe_offload_async).  Call copies_join before reusing or
+    releasing `dev_tensor`."""
+    n = _host_pair(host, dev_tensor, "offload")
+    _check(lib().upipe_offload_async(ctypes.c_void_p(host.data_ptr()), ctypes.c_void_p(dev_tensor.data_ptr()), n,
+                                     _stream(stream)), "upipe_offload_async")
+
+
+def prefetch_async(dev_tensor, host, stream=None) -> None:
+    """Copies the host tensor `host` into `dev_tensor` on the library's copy
+    stream, after the work already on `stream` (upipe_prefetch_async).  Call
+    copies_join before using `dev_tensor`."""
+    n = _host_pair(host, dev_tensor, "prefetch")
+    _check(lib().upipe_prefetch_async(ctypes.c_void_p(dev_tensor.data_ptr()), ctypes.c_void_p(host.data_ptr()), n,
+                                      _stream(stream)), "upipe_prefetch_async")
+
+
+def copies_join(stream=None) -> None:
+    """Work enqueued on `stream` afterwards waits for every offload and
+    prefetch issued so far on the current device (upipe_copies_join)."""
+    _check(lib().upipe_copies_join(_stream(stream)), "upipe_copies_join")
 
 
 def last_device_status(stream=None) -> int:

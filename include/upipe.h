@@ -55,6 +55,8 @@
  *    the work enqueued on `stream` before it, and work enqueued on `stream`
  *    after it waits for all of it.  Make the first backward call on each
  *    device outside stream capture.
+ *  - The activation-offload calls below use two more library-owned streams
+ *    per device (copies to and from the host), created on their first use.
  *  - Entry points may be called from several host threads (calls that share
  *    a workspace still need GPU ordering); the launch counter and the
  *    profiling hooks below are meant for one thread.
@@ -212,6 +214,32 @@ int upipe_attn_core_bwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t*
 int upipe_attn_core_bwd_noalloc(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const uint16_t* o, const float* lse, const uint16_t* dout_o, uint16_t* dq,
                                 uint16_t* dk, uint16_t* dv, void* stream);
+
+/* Activation offload ("Untied Ulysses Pushes Llama-3-8B Training to 5
+ * Million Tokens", paragraph on activation offloading): a block input that
+ * the backward pass needs and that cannot be cheaply recomputed -- for this
+ * layer, x -- is moved to CPU memory while it is not needed and prefetched
+ * before the backward pass reaches the layer, with the copies scheduled
+ * around the computation.  On GB300 the host memory sits behind the
+ * NVLink-C2C link.
+ *   upipe_offload_async(host_dst, dev_src, bytes, stream)   device -> host
+ *   upipe_prefetch_async(dev_dst, host_src, bytes, stream)  host -> device
+ *     Each copy runs on a library-owned copy stream of the current device
+ *     (one per direction, created on the first call there; make that first
+ *     call outside stream capture), after all work enqueued on `stream`
+ *     before the call, and returns without waiting.  Host buffers should be
+ *     page-locked (cudaHostAlloc / pinned) for the copy to be asynchronous.
+ *   upipe_copies_join(stream)
+ *     Work enqueued on `stream` after this call waits for every copy issued
+ *     so far on the current device (in both directions).  Join before
+ *     overwriting or releasing an offloaded source, and before using a
+ *     prefetched destination.
+ * Return UPIPE_OK, UPIPE_ERR_INVALID_ARG (null pointer with bytes > 0) or
+ * UPIPE_ERR_CUDA.  bytes == 0 is a no-op.  No counterpart of these calls
+ * has its own device kernel: the copy engines move the bytes.             */
+int upipe_offload_async(void* host_dst, const void* dev_src, size_t bytes, void* stream);
+int upipe_prefetch_async(void* dev_dst, const void* host_src, size_t bytes, void* stream);
+int upipe_copies_join(void* stream);
 
 /* Synchronizes `stream`, then reads and clears the device status word of
  * the current device.  Returns UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT if a

@@ -227,3 +227,11 @@ def test_binding_rejects_mis_shaped_or_mis_typed_tensors_before_any_launch(lib):
     with pytest.raises(ValueError, match="Wqkv"):
         upipe.attn_fwd(lcfg, x, w[:512], wo, x, lse)
     assert upipe.launch_count() == n0
+
+
+def test_offload_entry_points_reject_null_buffers_before_any_copy(lib):
+    """A zero-byte copy is a no-op and a null buffer with bytes > 0 is an
+    argument error; neither reaches the CUDA runtime."""
+    assert lib.upipe_prefetch_async(None, None, 0, None) == upipe.UPIPE_OK
+    assert lib.upipe_prefetch_async(None, ctypes.c_void_p(1 << 20), 64, None) == upipe.UPIPE_ERR_INVALID_ARG
+    assert lib.upipe_offload_async(ctypes.c_void_p(1 << 20), None, 64, None) == upipe.UPIPE_ERR_INVALID_ARG

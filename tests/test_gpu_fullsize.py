@@ -18,8 +18,10 @@ chunk size and by the small-size full parity tests.
 """
 
 import math
+import os
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -128,20 +130,30 @@ def _fwd_rows(Q, K, V, rows, g, scale):
 
 
 def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
-    """dQ, dK, dV of the last T positions (RoPE undone on dQ, dK)."""
+    """dQ, dK, dV of the last T positions (RoPE undone on dQ, dK).  Heads are
+    independent, so they run on a thread pool (NumPy releases the GIL in its
+    matrix products and element-wise loops); each head's dK/dV share is
+    summed into its KV head afterwards, in head order."""
     T, H = Qt.shape[0], Qt.shape[1]
     Hkv = K.shape[1]
     rnd = orc.bf16_round if bf else (lambda a: a)
     dq = np.empty((T, H, D_HEAD))
     dk = np.zeros((T, Hkv, D_HEAD))
     dv = np.zeros((T, Hkv, D_HEAD))
-    for h in range(H):
+
+    def head(h):
         kh, vh = K[:, h // g], V[:, h // g]
         # O recomputed from the LSE, as the backward does
         o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, p_bf16=bf)
         o_t = rnd(o_t)
-        dq[:, h] = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
+        dq_h = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
         a, b = orc.attention_dkv_tail(Qt[:, h], kh[tpos], vh[tpos], dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
+        return dq_h, a, b
+
+    with ThreadPoolExecutor(max_workers=min(H, os.cpu_count() or 1)) as ex:
+        parts = list(ex.map(head, range(H)))
+    for h, (dq_h, a, b) in enumerate(parts):
+        dq[:, h] = dq_h
         dk[:, h // g] += a
         dv[:, h // g] += b
     dq = orc.rope_apply(dq, tpos, theta, inverse=True)
@@ -328,9 +340,10 @@ def test_long_context_sweep_layer_L1M_and_L2M(monkeypatch):
     big = synth.LayerShape(L=1 << 21, D=4096, H=32, Hkv=8, U=4)
     xd_all, wd, wod, dd_all = synth.layer_inputs(big, device="cuda:0")
     x, w, wo, dout = (t.cpu() for t in (xd_all, wd, wod, dd_all))
-    # One oracle block per head for the sampled rows (the streamed blocking
-    # changes no result: see the oracle pins).
-    monkeypatch.setattr(orc, "ROW_BLOCK", 256)
+    # Sampled rows in blocks of 32 per head (the streamed blocking changes no
+    # result: see the oracle pins), so that the heads running in parallel
+    # in _tail each hold a few 32 x L score blocks.
+    monkeypatch.setattr(orc, "ROW_BLOCK", 32)
     # The fp64 K/V projection of all 2M rows (CPU) runs on a second thread
     # while the GPU runs below: BLAS and CUDA waits both release the GIL.
     kv = {}
