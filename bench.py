@@ -55,6 +55,11 @@ U_SWEEP = {
     "llama3_8b_layer_L262144_U4": (32, 8, 4),
 }
 TARGET_FRAC_OF_BURST = 0.55
+O_MODE_NOTE = {
+    "host": "kept in page-locked host memory: each chunk's O copied out during the forward and back during "
+            "the backward on copy streams, inside the timed step; the backward does not recompute it",
+    "recompute": "recomputed by the backward from the forward's LSE (a second pass over the keys)",
+}
 # Kernel kinds that are not attention: they run one at a time on the
 # caller's stream, so their event times add up to the step's projection time.
 PROJ_KINDS = ("rope_table", "qkv_gemm", "oproj_gemm", "do_gemm", "dwo_gemm", "dwqkv_gemm", "dx_gemm", "delta",
@@ -336,13 +341,27 @@ def run_upipe(args, w, world, rank, local):
     dx = torch.empty((L, D), dtype=torch.bfloat16, device=dev)
     dwqkv = torch.empty(((H + 2 * Hkv) * 128, D), dtype=torch.float32, device=dev)
     dwo = torch.empty((D, H * 128), dtype=torch.float32, device=dev)
-    ws_bytes = max(upipe.workspace_bytes(cfg, 0), upipe.workspace_bytes(cfg, 1))
+    # Where O waits between forward and backward: "recompute" (the
+    # backward recomputes it from the LSE) or "host" (kept in page-locked
+    # host memory, two chunk buffers on the device).  The other mode is
+    # timed too and reported beside the line.
+    modes = (args.o_mode, "host" if args.o_mode == "recompute" else "recompute")
+    o_code = {"recompute": upipe.O_RECOMPUTE, "host": upipe.O_HOST}
+    ws_bytes = max(upipe.workspace_bytes(cfg, p, o_mode=o_code[m]) for p in (0, 1) for m in modes)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o_host = upipe.new_host_o(cfg)
     torch.cuda.synchronize(dev)
 
-    def step():
-        upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream)
-        upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream)
+    def layer_step(mode, bx, bw, bwo, bd, bo, bl, bdx, bdw, bdwo):
+        if mode == "host":
+            upipe.attn_fwd_host_o(cfg, bx, bw, bwo, bo, bl, o_host, ws, stream)
+            upipe.attn_bwd_host_o(cfg, bx, bw, bwo, bd, bl, o_host, bdx, bdw, bdwo, ws, stream)
+        else:
+            upipe.attn_fwd(cfg, bx, bw, bwo, bo, bl, None, ws, stream)
+            upipe.attn_bwd(cfg, bx, bw, bwo, bd, bl, bdx, bdw, bdwo, None, ws, stream)
+
+    def step(mode=args.o_mode):
+        layer_step(mode, x, wqkv, wo, dout, out, lse, dx, dwqkv, dwo)
 
     def barrier():
         if world > 1:
@@ -403,15 +422,25 @@ def run_upipe(args, w, world, rank, local):
         torch.cuda.synchronize(dev)
         return a0.elapsed_time(a1) / n
     n_split = max(1, min(args.steps, 3))
-    fwd_ms = timed(lambda: upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream), n_split)
-    bwd_ms = timed(lambda: upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream), n_split)
+    if args.o_mode == "host":
+        fwd_ms = timed(lambda: upipe.attn_fwd_host_o(cfg, x, wqkv, wo, out, lse, o_host, ws, stream), n_split)
+        bwd_ms = timed(lambda: upipe.attn_bwd_host_o(cfg, x, wqkv, wo, dout, lse, o_host, dx, dwqkv, dwo, ws,
+                                                     stream), n_split)
+    else:
+        fwd_ms = timed(lambda: upipe.attn_fwd(cfg, x, wqkv, wo, out, lse, None, ws, stream), n_split)
+        bwd_ms = timed(lambda: upipe.attn_bwd(cfg, x, wqkv, wo, dout, lse, dx, dwqkv, dwo, None, ws, stream),
+                       n_split)
     check_status("after the fwd/bwd split")
+    # The other O mode, same inputs, a few steps.
+    other_mode = modes[1]
+    other_ms = timed(lambda: step(other_mode), n_split)
+    check_status("after the other O mode")
 
     attn_f, proj_f = layer_flops(L, D, H, Hkv)
     step_flops = attn_f + proj_f
-    # Hardware work adds the backward's recompute of the QKV slices and of the
-    # attention forward (the forward's share of attn_f is 2 of its 7 parts).
-    recompute_flops = attn_f * 2.0 / 7.0 + 2.0 * L * D * (H + 2 * Hkv) * 128
+    # Hardware work adds the backward's recompute of the QKV slices and, when
+    # O is not kept, of the attention forward (2 of attn_f's 7 parts).
+    recompute_flops = (attn_f * 2.0 / 7.0 if args.o_mode == "recompute" else 0.0) + 2.0 * L * D * (H + 2 * Hkv) * 128
     ms_step = ms / args.steps
     value = job_tflops(step_flops, ms_step, world)
     burst, sustained, hbm, peak_src = peaks()
@@ -483,8 +512,7 @@ def run_upipe(args, w, world, rank, local):
         def compute(b):
             bx, bw, bwo, bd, bo, bl, bdx, bdw, bdwo = sets[b]
             stream.wait_event(ready[b])
-            upipe.attn_fwd(cfg, bx, bw, bwo, bo, bl, None, ws, stream)
-            upipe.attn_bwd(cfg, bx, bw, bwo, bd, bl, bdx, bdw, bdwo, None, ws, stream)
+            layer_step(args.o_mode, bx, bw, bwo, bd, bo, bl, bdx, bdw, bdwo)
             done[b].record(stream)
             s_out.wait_event(done[b])
             with torch.cuda.stream(s_out):
@@ -556,7 +584,7 @@ def run_upipe(args, w, world, rank, local):
         check_status("after the offload measurement")
 
     # ---- peak activation bytes and throughput against U (measured)
-    del ws
+    del ws, o_host
     sweep = None
     if not args.no_u_sweep:
         sweep = u_sweep(w, U_SWEEP.get(args.workload, (H, U)), dev, stream, x, wqkv, wo, dout)
@@ -576,7 +604,7 @@ def run_upipe(args, w, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, **w, "d": 128, "rope_theta": 500000.0, "causal": True,
-                   "o_saved": False, "flops_per_step": step_flops, "attn_flops_per_step": attn_f,
+                   "o": O_MODE_NOTE[args.o_mode], "flops_per_step": step_flops, "attn_flops_per_step": attn_f,
                    "l2": (f"inputs larger than L2 (x, dout {L * D * 2 / 2**20:.0f} MiB each)" if 2 * L * D * 2 > 129e6
                           else f"inputs fit in L2 (x, dout {L * D * 2 / 2**20:.1f} MiB each; not flushed)"),
                    "parallelism": f"replicas x{world}"},
@@ -588,7 +616,10 @@ def run_upipe(args, w, world, rank, local):
                     "fwd_tflops": world * (attn_f * 2.0 / 7.0 + proj_f / 3.0) / (fwd_ms / 1e3) / 1e12,
                     "bwd_tflops": world * (attn_f * 5.0 / 7.0 + proj_f * 2.0 / 3.0) / (bwd_ms / 1e3) / 1e12},
         "hfu": {"value": world * (step_flops + recompute_flops) / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
-                "note": "hardware flops: the layer flops plus the backward's recompute of QKV and attention fwd"},
+                "note": "hardware flops: the layer flops plus the backward's recompute of QKV"
+                        + (" and attention fwd" if args.o_mode == "recompute" else "")},
+        "other_o_mode": {"o": O_MODE_NOTE[other_mode], "ms_per_step": other_ms,
+                         "value": job_tflops(step_flops, other_ms, world), "steps": n_split},
         "roofline": roofline, "kernels": kernels, "profiled_step_ms": prof_step_ms,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clocks, "u_sweep": sweep, "offload": offload,
@@ -614,6 +645,8 @@ def main():
     ap.add_argument("--cpu-sample-L", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-u-sweep", action="store_true")
+    ap.add_argument("--o-mode", default="host", choices=["host", "recompute"],
+                    help="where the attention output O waits between forward and backward")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     env_world = os.environ.get("WORLD_SIZE")

@@ -72,13 +72,21 @@ struct Plan {
   size_t fixed_bytes() const { return carry32 + rope; }
 };
 
+// Where the layer entries keep the attention output O between the forward
+// and the backward.
+enum OMode {
+  kOWorkspace = 0,  // O_c lives in the workspace; the backward recomputes it
+  kODevice = 1,     // the caller's o_saved [L, H*128] holds every chunk's O
+  kOHost = 2,       // page-locked host memory holds it; two chunk buffers stage the copies
+};
+
 // LSE/Delta records of the backward: per head of the chunk and 64-query
 // tile, 64 -LSE*log2(e) then 64 Delta floats.
 size_t ld_records_bytes(const Shape& s) {
   return static_cast<size_t>(s.U) * static_cast<size_t>((s.L + 63) / 64) * 128 * sizeof(float);
 }
 
-Plan make_plan(const Shape& s, int pass, bool core, bool o_saved) {
+Plan make_plan(const Shape& s, int pass, bool core, int o_mode) {
   Plan p;
   const size_t L = static_cast<size_t>(s.L);
   const size_t slot = L * kHeadDim * 2;  // one head-major [L, 128] bf16 buffer
@@ -91,7 +99,8 @@ Plan make_plan(const Shape& s, int pass, bool core, bool o_saved) {
   } else {
     p.rope = L * 64 * sizeof(float2);
     p.qkv = (s.U + 2 * s.kvc) * slot;
-    if (!o_saved) p.o = s.U * slot;
+    if (o_mode == kOWorkspace) p.o = s.U * slot;
+    if (o_mode == kOHost) p.o = 2 * s.U * slot;
     if (s.nch > 1) p.carry32 = L * s.D * 4;
     if (pass == 1) {
       p.dO = s.U * slot;
@@ -306,10 +315,13 @@ int launch_attn_bwd_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 // Copy streams of the activation offload: one per direction and device,
 // created on first use, with an event to order each batch of copies after
-// the caller's stream and one per direction to join them back.
+// the caller's stream and one per direction to join them back.  o_ready and
+// o_done[2] order the layer entries' copies of O to and from host memory
+// (o_done[b]: the last copy through chunk buffer b).
 struct Copier {
   cudaStream_t d2h = nullptr, h2d = nullptr;
   cudaEvent_t after = nullptr, done_d2h = nullptr, done_h2d = nullptr;
+  cudaEvent_t o_ready = nullptr, o_done[2] = {nullptr, nullptr};
 };
 Copier g_copier[kMaxDev];
 std::mutex g_copier_mu;
@@ -327,8 +339,8 @@ int copier(Copier** out) {
     if (!c.h2d && cudaStreamCreateWithPriority(&c.h2d, cudaStreamNonBlocking, least) != cudaSuccess)
       return UPIPE_ERR_CUDA;
     if (!c.after && cudaEventCreateWithFlags(&c.after, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
-    if (!c.done_d2h && cudaEventCreateWithFlags(&c.done_d2h, cudaEventDisableTiming) != cudaSuccess)
-      return UPIPE_ERR_CUDA;
+    for (cudaEvent_t* e : {&c.done_d2h, &c.o_ready, &c.o_done[0], &c.o_done[1]})
+      if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
     if (cudaEventCreateWithFlags(&c.done_h2d, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
   }
   *out = &c;
@@ -356,6 +368,30 @@ int async_copy(void* dst, const void* src, size_t bytes, bool to_host, cudaStrea
     if (!(x)) return UPIPE_ERR_CUDA;                 \
   } while (0)
 
+// Page-locked (or registered) host memory: the only kind a copy stream
+// copies without blocking the calling thread.
+bool host_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+// One chunk's O ([L, U*128] bf16) between a workspace buffer and its block
+// of host memory, on the direction's copy stream after everything enqueued
+// on st so far; o_done[buf] marks its end.
+int copy_o_chunk(Copier* cp, void* dst, const void* src, size_t bytes, bool to_host, int buf, cudaStream_t st) {
+  cudaStream_t cs = to_host ? cp->d2h : cp->h2d;
+  if (cudaEventRecord(cp->o_ready, st) != cudaSuccess || cudaStreamWaitEvent(cs, cp->o_ready, 0) != cudaSuccess ||
+      cudaMemcpyAsync(dst, src, bytes, to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, cs) !=
+          cudaSuccess ||
+      cudaEventRecord(cp->o_done[buf], cs) != cudaSuccess)
+    return UPIPE_ERR_CUDA;
+  return UPIPE_OK;
+}
+
 using bf16 = __nv_bfloat16;
 
 GemmParams gemm_base(int* status, uint64_t limit) {
@@ -379,61 +415,28 @@ int w_block(const Shape& s, const Chunk& ch, int sl) {
   return s.H + s.Hkv + ch.kv0 + (sl - s.U - s.kvc);
 }
 
-}  // namespace
-}  // namespace upipe
-
-using namespace upipe;
-
-extern "C" {
-
-size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved) {
-  Shape s;
-  if ((pass != 0 && pass != 1) || !check_cfg(cfg, !core_only, &s)) return 0;
-  return make_plan(s, pass, core_only != 0, has_o_saved != 0).total;
-}
-
-int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved, size_t* chunk_bytes,
-                           size_t* fixed_bytes) {
-  Shape s;
-  if ((pass != 0 && pass != 1) || !check_cfg(cfg, !core_only, &s)) return UPIPE_ERR_INVALID_ARG;
-  const Plan p = make_plan(s, pass, core_only != 0, has_o_saved != 0);
-  if (chunk_bytes) *chunk_bytes = p.chunk_bytes();
-  if (fixed_bytes) *fixed_bytes = p.fixed_bytes();
-  return UPIPE_OK;
-}
-
-int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int has_o_saved) {
-  if (!cfg || pass < 0 || pass > 2) return UPIPE_ERR_INVALID_ARG;
-  upipe_cfg c = *cfg;
-  Shape s;
-  c.U = c.H;  // U = H is valid whenever the rest of the configuration is
-  if (!check_cfg(&c, !core_only, &s)) return UPIPE_ERR_INVALID_ARG;
-  for (int u = c.H; u >= 1; --u) {
-    c.U = u;
-    if (!check_cfg(&c, !core_only, &s)) continue;
-    size_t need = 0;
-    for (int ps = 0; ps < 2; ++ps)
-      if (pass == 2 || pass == ps) {
-        const size_t b = make_plan(s, ps, core_only != 0, has_o_saved != 0).total;
-        need = b > need ? b : need;
-      }
-    if (need <= budget_bytes) return u;
-  }
-  return UPIPE_ERR_WS_TOO_SMALL;
-}
-
-int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo, uint16_t* out,
-                   float* lse, uint16_t* o_saved, void* ws, size_t ws_bytes, void* stream) {
+// Layer forward; at most one of o_saved (device) and o_host (page-locked
+// host memory) is non-null.
+int layer_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo, uint16_t* out,
+              float* lse, uint16_t* o_saved, uint16_t* o_host, void* ws, size_t ws_bytes, void* stream) {
   Shape s;
   if (!check_cfg(cfg, true, &s)) return UPIPE_ERR_INVALID_ARG;
   if (!x || !Wqkv || !Wo || !out || !lse || !ws) return UPIPE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out) || !aligned16(lse) ||
       !aligned16(ws) || (o_saved && !aligned16(o_saved)))
     return UPIPE_ERR_INVALID_ARG;
-  const Plan pl = make_plan(s, 0, false, o_saved != nullptr);
+  const int o_mode = o_host ? kOHost : o_saved ? kODevice : kOWorkspace;
+  const Plan pl = make_plan(s, 0, false, o_mode);
   if (ws_bytes < pl.total) return UPIPE_ERR_WS_TOO_SMALL;
   int* status = nullptr;
   if (int e = device_ready(&status)) return e;
+  // The O copies use the shared copy streams and events: one call at a time.
+  std::unique_lock<std::mutex> copy_lock;
+  Copier* cp = nullptr;
+  if (o_host) {
+    copy_lock = std::unique_lock<std::mutex>(g_copier_mu);
+    if (int e = copier(&cp)) return e;
+  }
   const uint64_t limit = spin_limit_ns();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -452,7 +455,10 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
   UPIPE_MAP(map3d(&m_qkv, qkv, L, slots, 128, L * 128, 128));
   const bf16* obuf = o_saved ? reinterpret_cast<const bf16*>(o_saved) : reinterpret_cast<bf16*>(w + pl.off_o);
   const int64_t ld_o = o_saved ? static_cast<int64_t>(s.H) * 128 : static_cast<int64_t>(s.U) * 128;
+  const size_t o_chunk_elems = static_cast<size_t>(L) * s.U * 128;  // one chunk buffer of O
   UPIPE_MAP(map2d(&m_o, obuf, ld_o, L, ld_o, 128));
+  CUtensorMap m_o1;  // host mode: the second chunk buffer
+  if (o_host) UPIPE_MAP(map2d(&m_o1, obuf + o_chunk_elems, ld_o, L, ld_o, 128));
   UPIPE_MAP(map2d(&m_wo, Wo, static_cast<uint64_t>(s.H) * 128, s.D, static_cast<uint64_t>(s.H) * 128, 128));
 
   for (int c = 0; c < s.nch; ++c) {
@@ -474,7 +480,11 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
 
     // a-3: causal attention.  A kept O is written from the final
     // probabilities (LSE first, then O from it): the same bits the
-    // backward's recomputation of O produces.
+    // backward's recomputation of O produces.  O bound for host memory is
+    // the online softmax's own output, staged in chunk buffer c % 2 once
+    // the copy of chunk c - 2 has left it.
+    const int buf = o_host ? (c & 1) : 0;
+    if (o_host && c >= 2) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[buf], 0));
     AttnFwdParams a;
     std::memset(&a, 0, sizeof(a));
     a.L = static_cast<int>(L);
@@ -483,7 +493,7 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     a.q_z0 = 0;
     a.k_z0 = s.U;
     a.v_z0 = s.U + s.kvc;
-    a.o = const_cast<bf16*>(obuf) + (o_saved ? static_cast<int64_t>(ch.q0) * 128 : 0);
+    a.o = const_cast<bf16*>(obuf) + (o_saved ? static_cast<int64_t>(ch.q0) * 128 : buf * o_chunk_elems);
     a.o_row = ld_o;
     a.o_head = 128;
     a.lse = lse + static_cast<int64_t>(ch.q0) * L;
@@ -499,6 +509,9 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
       a.write_lse = 0;
     }
     UPIPE_LAUNCH(UPIPE_KIND_ATTN_FWD, launch_attn_fwd(m_qkv, m_qkv, m_qkv, a, m_tiles, st));
+    if (o_host) {
+      if (int e = copy_o_chunk(cp, o_host + c * o_chunk_elems, a.o, o_chunk_elems * 2, true, buf, st)) return e;
+    }
 
     // a-4: out32 (+)= O_c Wo[:, cols_c]^T; the last chunk writes bf16 out.
     GemmParams o = gemm_base(status, limit);
@@ -515,24 +528,34 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     o.carry = carry;
     o.carry_in = c > 0;
     o.final_out = c == s.nch - 1;
-    UPIPE_LAUNCH(UPIPE_KIND_OPROJ_GEMM, launch_gemm(GK_OPROJ, m_o, m_wo, o, st));
+    UPIPE_LAUNCH(UPIPE_KIND_OPROJ_GEMM, launch_gemm(GK_OPROJ, buf ? m_o1 : m_o, m_wo, o, st));
   }
+  // Host O complete when the caller's stream passes this point.
+  if (o_host) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[(s.nch - 1) & 1], 0));
   return UPIPE_OK;
 }
 
-int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
-                   const uint16_t* dout, const float* lse, const uint16_t* o_saved, uint16_t* dx, float* dWqkv,
-                   float* dWo, void* ws, size_t ws_bytes, void* stream) {
+// Layer backward; at most one of o_saved and o_host is non-null.
+int layer_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+              const uint16_t* dout, const float* lse, const uint16_t* o_saved, const uint16_t* o_host, uint16_t* dx,
+              float* dWqkv, float* dWo, void* ws, size_t ws_bytes, void* stream) {
   Shape s;
   if (!check_cfg(cfg, true, &s)) return UPIPE_ERR_INVALID_ARG;
   if (!x || !Wqkv || !Wo || !dout || !lse || !dx || !dWqkv || !dWo || !ws) return UPIPE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(dout) || !aligned16(lse) ||
       !aligned16(dx) || !aligned16(dWqkv) || !aligned16(dWo) || !aligned16(ws) || (o_saved && !aligned16(o_saved)))
     return UPIPE_ERR_INVALID_ARG;
-  const Plan pl = make_plan(s, 1, false, o_saved != nullptr);
+  const int o_mode = o_host ? kOHost : o_saved ? kODevice : kOWorkspace;
+  const Plan pl = make_plan(s, 1, false, o_mode);
   if (ws_bytes < pl.total) return UPIPE_ERR_WS_TOO_SMALL;
   int* status = nullptr;
   if (int e = device_ready(&status)) return e;
+  std::unique_lock<std::mutex> copy_lock;
+  Copier* cp = nullptr;
+  if (o_host) {
+    copy_lock = std::unique_lock<std::mutex>(g_copier_mu);
+    if (int e = copier(&cp)) return e;
+  }
   const uint64_t limit = spin_limit_ns();
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -554,6 +577,9 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
 
   const bf16* obuf = o_saved ? reinterpret_cast<const bf16*>(o_saved) : reinterpret_cast<bf16*>(w + pl.off_o);
   const int64_t ld_o = o_saved ? Hd : static_cast<int64_t>(s.U) * 128;
+  const size_t o_chunk_elems = static_cast<size_t>(L) * s.U * 128;
+  CUtensorMap m_o1_mn;  // host mode: the second chunk buffer
+  if (o_host) UPIPE_MAP(map2d(&m_o1_mn, obuf + o_chunk_elems, ld_o, L, ld_o, 64));
   CUtensorMap m_x, m_xmn, m_wqkv, m_wqkv_mn, m_qkv, m_wo_mn, m_dout, m_dout_mn, m_o_mn, m_do,
       m_dqkv_k, m_dqkv_mn;
   UPIPE_MAP(map2d(&m_x, x, s.D, L, s.D, 128));
@@ -569,6 +595,14 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
   UPIPE_MAP(map3d(&m_dqkv_k, dqkv, L, 2 * slots, 128, L * 128, 128));
   UPIPE_MAP(map3d(&m_dqkv_mn, dqkv, L, 2 * slots, 128, L * 128, 64));
 
+  // Host mode: chunk c's O comes back into buffer c % 2.  The copy of
+  // chunk c + 1 is issued once everything of chunk c - 1 (the last reader of
+  // that buffer) is enqueued, and runs under chunk c's work.
+  const bf16* oh = reinterpret_cast<const bf16*>(o_host);
+  auto o_chunk = [&](int c) { return const_cast<bf16*>(obuf) + (c & 1) * o_chunk_elems; };
+  if (o_host) {
+    if (int e = copy_o_chunk(cp, o_chunk(0), oh, o_chunk_elems * 2, false, 0, st)) return e;
+  }
   const int chunks_per_group = s.U < s.g ? s.g / s.U : 1;
   for (int c = 0; c < s.nch; ++c) {
     const Chunk ch = chunk_of(s, c);
@@ -576,6 +610,11 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     const bool group_first = cg == 0;
     const bool group_last = cg == chunks_per_group - 1;
     const bool emit_kv = group_last;  // K/V gradients complete for this chunk's KV heads
+    if (o_host && c + 1 < s.nch) {
+      if (int e = copy_o_chunk(cp, o_chunk(c + 1), oh + (c + 1) * o_chunk_elems, o_chunk_elems * 2, false,
+                               (c + 1) & 1, st))
+        return e;
+    }
 
     // Recompute Q/K/V of the chunk (a-1, a-2).
     GemmParams g = gemm_base(status, limit);
@@ -595,7 +634,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     // Recompute O_c unless the caller kept it (a-3), from the forward's LSE:
     // the probabilities are final at once, and are the ones the backward
     // kernels use.
-    if (!o_saved) {
+    if (!o_saved && !o_host) {
       AttnFwdParams a;
       std::memset(&a, 0, sizeof(a));
       a.mode = kLseIn;
@@ -616,6 +655,8 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
       UPIPE_LAUNCH(UPIPE_KIND_ATTN_FWD, launch_attn_fwd(m_qkv, m_qkv, m_qkv, a, m_tiles, st));
     }
     const int o_col0 = o_saved ? ch.q0 * 128 : 0;
+    const bf16* o_rows = o_host ? o_chunk(c) : obuf + o_col0;
+    if (o_host) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[c & 1], 0));  // O_c is back
 
     // dO_c = dout Wo[:, cols_c], and Delta = rowsum(dO_c * O_c).
     GemmParams d = gemm_base(status, limit);
@@ -628,7 +669,7 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     d.b_col0 = ch.q0 * 128;
     d.L = static_cast<int>(L);
     d.out = dO;
-    d.o_rows = obuf + o_col0;
+    d.o_rows = o_rows;
     d.ld_o = ld_o;
     d.lse_in = lse + static_cast<int64_t>(ch.q0) * L;
     d.ld_rec = delta;
@@ -655,7 +696,8 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
       UPIPE_LAUNCH(UPIPE_KIND_ZERO_ROWS,
                    launch_zero_rows(dWo + dw.out_col0, Hd, dw.N, rows, dw.m_tiles, st));
     }
-    UPIPE_LAUNCH(UPIPE_KIND_DWO_GEMM, launch_gemm(GK_DWO, m_dout_mn, m_o_mn, dw, st));
+    UPIPE_LAUNCH(UPIPE_KIND_DWO_GEMM,
+                 launch_gemm(GK_DWO, m_dout_mn, o_host && (c & 1) ? m_o1_mn : m_o_mn, dw, st));
 
     // Attention backward (a-5): dQ, then dK/dV (carried when U < g).
     AttnBwdParams b;
@@ -745,6 +787,74 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
     UPIPE_LAUNCH(UPIPE_KIND_DX_GEMM, launch_gemm(GK_DX, m_dqkv_k, m_wqkv_mn, dxp, st));
   }
   return UPIPE_OK;
+}
+
+}  // namespace
+}  // namespace upipe
+
+using namespace upipe;
+
+extern "C" {
+
+size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int o_mode) {
+  Shape s;
+  if ((pass != 0 && pass != 1) || o_mode < 0 || o_mode > 2 || !check_cfg(cfg, !core_only, &s)) return 0;
+  return make_plan(s, pass, core_only != 0, o_mode).total;
+}
+
+int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int o_mode, size_t* chunk_bytes,
+                           size_t* fixed_bytes) {
+  Shape s;
+  if ((pass != 0 && pass != 1) || o_mode < 0 || o_mode > 2 || !check_cfg(cfg, !core_only, &s))
+    return UPIPE_ERR_INVALID_ARG;
+  const Plan p = make_plan(s, pass, core_only != 0, o_mode);
+  if (chunk_bytes) *chunk_bytes = p.chunk_bytes();
+  if (fixed_bytes) *fixed_bytes = p.fixed_bytes();
+  return UPIPE_OK;
+}
+
+int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int o_mode) {
+  if (!cfg || pass < 0 || pass > 2 || o_mode < 0 || o_mode > 2) return UPIPE_ERR_INVALID_ARG;
+  upipe_cfg c = *cfg;
+  Shape s;
+  c.U = c.H;  // U = H is valid whenever the rest of the configuration is
+  if (!check_cfg(&c, !core_only, &s)) return UPIPE_ERR_INVALID_ARG;
+  for (int u = c.H; u >= 1; --u) {
+    c.U = u;
+    if (!check_cfg(&c, !core_only, &s)) continue;
+    size_t need = 0;
+    for (int ps = 0; ps < 2; ++ps)
+      if (pass == 2 || pass == ps) {
+        const size_t b = make_plan(s, ps, core_only != 0, o_mode).total;
+        need = b > need ? b : need;
+      }
+    if (need <= budget_bytes) return u;
+  }
+  return UPIPE_ERR_WS_TOO_SMALL;
+}
+
+int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo, uint16_t* out,
+                   float* lse, uint16_t* o_saved, void* ws, size_t ws_bytes, void* stream) {
+  return layer_fwd(cfg, x, Wqkv, Wo, out, lse, o_saved, nullptr, ws, ws_bytes, stream);
+}
+
+int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                   const uint16_t* dout, const float* lse, const uint16_t* o_saved, uint16_t* dx, float* dWqkv,
+                   float* dWo, void* ws, size_t ws_bytes, void* stream) {
+  return layer_bwd(cfg, x, Wqkv, Wo, dout, lse, o_saved, nullptr, dx, dWqkv, dWo, ws, ws_bytes, stream);
+}
+
+int upipe_attn_fwd_host_o(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                          uint16_t* out, float* lse, uint16_t* o_host, void* ws, size_t ws_bytes, void* stream) {
+  if (!o_host || !host_pinned(o_host)) return UPIPE_ERR_INVALID_ARG;
+  return layer_fwd(cfg, x, Wqkv, Wo, out, lse, nullptr, o_host, ws, ws_bytes, stream);
+}
+
+int upipe_attn_bwd_host_o(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                          const uint16_t* dout, const float* lse, const uint16_t* o_host, uint16_t* dx, float* dWqkv,
+                          float* dWo, void* ws, size_t ws_bytes, void* stream) {
+  if (!o_host || !host_pinned(o_host)) return UPIPE_ERR_INVALID_ARG;
+  return layer_bwd(cfg, x, Wqkv, Wo, dout, lse, nullptr, o_host, dx, dWqkv, dWo, ws, ws_bytes, stream);
 }
 
 int upipe_attn_core_fwd(const upipe_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,

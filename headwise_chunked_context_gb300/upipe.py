@@ -26,6 +26,7 @@ UPIPE_ERR_DEVICE_TIMEOUT = -4
 UPIPE_ERR_UNSUPPORTED_DEVICE = -5
 UPIPE_ERR_SCRATCH_LIMIT = -6
 NOALLOC_SCRATCH_BYTES = 32 << 20
+O_RECOMPUTE, O_DEVICE, O_HOST = 0, 1, 2  # where the layer keeps O between forward and backward
 
 EXPORTS = (
     "upipe_workspace_bytes",
@@ -33,6 +34,8 @@ EXPORTS = (
     "upipe_choose_u",
     "upipe_attn_fwd",
     "upipe_attn_bwd",
+    "upipe_attn_fwd_host_o",
+    "upipe_attn_bwd_host_o",
     "upipe_attn_core_fwd",
     "upipe_attn_core_bwd",
     "upipe_attn_core_bwd_noalloc",
@@ -111,6 +114,10 @@ def lib() -> ctypes.CDLL:
         L.upipe_attn_fwd.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_bwd.restype = ctypes.c_int
         L.upipe_attn_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_fwd_host_o.restype = ctypes.c_int
+        L.upipe_attn_fwd_host_o.argtypes = [cfgp, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_attn_bwd_host_o.restype = ctypes.c_int
+        L.upipe_attn_bwd_host_o.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_core_fwd.restype = ctypes.c_int
         L.upipe_attn_core_fwd.argtypes = [cfgp, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_core_bwd.restype = ctypes.c_int
@@ -198,34 +205,36 @@ def _expect_ws(ws, need, name="ws"):
 
 # ----------------------------------------------------------- raw entry points
 
-def workspace_bytes(cfg: Config, pass_: int, core_only: bool = False, has_o_saved: bool = False) -> int:
+def workspace_bytes(cfg: Config, pass_: int, core_only: bool = False, o_mode: int = O_RECOMPUTE) -> int:
+    """o_mode: O_RECOMPUTE, O_DEVICE (o_saved given) or O_HOST (the _host_o
+    entries); True / False read as O_DEVICE / O_RECOMPUTE."""
     c = cfg.c()
-    return int(lib().upipe_workspace_bytes(ctypes.byref(c), pass_, int(core_only), int(has_o_saved)))
+    return int(lib().upipe_workspace_bytes(ctypes.byref(c), pass_, int(core_only), int(o_mode)))
 
 
-def activation_bytes(cfg: Config, pass_: int, core_only: bool = False, has_o_saved: bool = False):
+def activation_bytes(cfg: Config, pass_: int, core_only: bool = False, o_mode: int = O_RECOMPUTE):
     c = cfg.c()
     chunk = ctypes.c_size_t(0)
     fixed = ctypes.c_size_t(0)
-    _check(lib().upipe_activation_bytes(ctypes.byref(c), pass_, int(core_only), int(has_o_saved),
+    _check(lib().upipe_activation_bytes(ctypes.byref(c), pass_, int(core_only), int(o_mode),
                                         ctypes.byref(chunk), ctypes.byref(fixed)), "upipe_activation_bytes")
     return int(chunk.value), int(fixed.value)
 
 
 def choose_u(cfg: Config, budget_bytes: int, pass_: int = 2, core_only: bool = False,
-             has_o_saved: bool = False) -> int:
+             o_mode: int = O_RECOMPUTE) -> int:
     """Largest valid chunk size U whose workspace fits `budget_bytes`
     (upipe_choose_u; cfg.U is ignored).  pass_ 0 = forward, 1 = backward,
     2 = the larger of the two.  Raises UpipeError when no U fits."""
     c = cfg.c()
-    r = int(lib().upipe_choose_u(ctypes.byref(c), int(budget_bytes), pass_, int(core_only), int(has_o_saved)))
+    r = int(lib().upipe_choose_u(ctypes.byref(c), int(budget_bytes), pass_, int(core_only), int(o_mode)))
     if r < 0:
         raise UpipeError(r, "upipe_choose_u")
     return r
 
 
-def _ws(cfg, pass_, core_only, has_o_saved, ws, device):
-    need = workspace_bytes(cfg, pass_, core_only, has_o_saved)
+def _ws(cfg, pass_, core_only, o_mode, ws, device):
+    need = workspace_bytes(cfg, pass_, core_only, o_mode)
     if ws is None:
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
     _expect_ws(ws, need)
@@ -263,7 +272,7 @@ def attn_fwd(cfg: Config, x, Wqkv, Wo, out, lse, o_saved=None, ws=None, stream=N
     _layer_tensors(cfg, x, Wqkv, Wo, lse, o_saved)
     _expect(out, (cfg.L, cfg.D), torch.bfloat16, "out")
     _on_device(x=x, Wqkv=Wqkv, Wo=Wo, out=out, lse=lse, o_saved=o_saved)
-    ws, nbytes = _ws(cfg, 0, False, o_saved is not None, ws, x.device)
+    ws, nbytes = _ws(cfg, 0, False, O_DEVICE if o_saved is not None else O_RECOMPUTE, ws, x.device)
     c = cfg.c()
     _check(lib().upipe_attn_fwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(out), _ptr(lse),
                                 _ptr(o_saved), _ptr(ws), nbytes, _stream(stream)), "upipe_attn_fwd")
@@ -277,11 +286,56 @@ def attn_bwd(cfg: Config, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved=None, 
     _expect(dWqkv, ((H + 2 * Hkv) * 128, D), torch.float32, "dWqkv")
     _expect(dWo, (D, H * 128), torch.float32, "dWo")
     _on_device(x=x, Wqkv=Wqkv, Wo=Wo, dout=dout, lse=lse, o_saved=o_saved, dx=dx, dWqkv=dWqkv, dWo=dWo)
-    ws, nbytes = _ws(cfg, 1, False, o_saved is not None, ws, x.device)
+    ws, nbytes = _ws(cfg, 1, False, O_DEVICE if o_saved is not None else O_RECOMPUTE, ws, x.device)
     c = cfg.c()
     _check(lib().upipe_attn_bwd(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(dout), _ptr(lse),
                                 _ptr(o_saved), _ptr(dx), _ptr(dWqkv), _ptr(dWo), _ptr(ws), nbytes,
                                 _stream(stream)), "upipe_attn_bwd")
+
+
+def _host_o(cfg: Config, o_host):
+    """o_host: a page-locked CPU tensor of L*H*128 bf16 (any shape)."""
+    if o_host is None:
+        raise ValueError("o_host: missing")
+    if o_host.is_cuda or o_host.dtype != torch.bfloat16 or o_host.numel() != cfg.L * cfg.H * 128:
+        raise ValueError(f"o_host: expected {cfg.L * cfg.H * 128} bf16 elements in host memory, got "
+                         f"{o_host.numel()} {o_host.dtype} on {o_host.device}")
+    if not o_host.is_contiguous() or not o_host.is_pinned():
+        raise ValueError("o_host: expected a contiguous page-locked (pinned) tensor")
+    return ctypes.c_void_p(o_host.data_ptr())
+
+
+def new_host_o(cfg: Config):
+    """Page-locked host buffer for upipe_attn_fwd_host_o: chunk c's O_c
+    [L, U*128] at element offset c*L*U*128."""
+    return torch.empty((cfg.H // cfg.U, cfg.L, cfg.U * 128), dtype=torch.bfloat16, pin_memory=True)
+
+
+def attn_fwd_host_o(cfg: Config, x, Wqkv, Wo, out, lse, o_host, ws=None, stream=None):
+    _layer_tensors(cfg, x, Wqkv, Wo, lse, None)
+    _expect(out, (cfg.L, cfg.D), torch.bfloat16, "out")
+    oh = _host_o(cfg, o_host)
+    _on_device(x=x, Wqkv=Wqkv, Wo=Wo, out=out, lse=lse)
+    ws, nbytes = _ws(cfg, 0, False, O_HOST, ws, x.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_fwd_host_o(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(out), _ptr(lse),
+                                       oh, _ptr(ws), nbytes, _stream(stream)), "upipe_attn_fwd_host_o")
+
+
+def attn_bwd_host_o(cfg: Config, x, Wqkv, Wo, dout, lse, o_host, dx, dWqkv, dWo, ws=None, stream=None):
+    L, D, H, Hkv = cfg.L, cfg.D, cfg.H, cfg.Hkv
+    _layer_tensors(cfg, x, Wqkv, Wo, lse, None)
+    _expect(dout, (L, D), torch.bfloat16, "dout")
+    _expect(dx, (L, D), torch.bfloat16, "dx")
+    _expect(dWqkv, ((H + 2 * Hkv) * 128, D), torch.float32, "dWqkv")
+    _expect(dWo, (D, H * 128), torch.float32, "dWo")
+    oh = _host_o(cfg, o_host)
+    _on_device(x=x, Wqkv=Wqkv, Wo=Wo, dout=dout, lse=lse, dx=dx, dWqkv=dWqkv, dWo=dWo)
+    ws, nbytes = _ws(cfg, 1, False, O_HOST, ws, x.device)
+    c = cfg.c()
+    _check(lib().upipe_attn_bwd_host_o(ctypes.byref(c), _ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(dout), _ptr(lse),
+                                       oh, _ptr(dx), _ptr(dWqkv), _ptr(dWo), _ptr(ws), nbytes,
+                                       _stream(stream)), "upipe_attn_bwd_host_o")
 
 
 def attn_core_fwd(cfg: Config, q, k, v, o, lse, ws=None, stream=None):
@@ -384,24 +438,35 @@ def profile_read():
 
 # ------------------------------------------------------- allocating helpers
 
-def layer_forward(cfg: Config, x, Wqkv, Wo, keep_o: bool = False):
-    """Allocates out [L, D] bf16, lse [H, L] fp32 (and O if keep_o) and runs
-    upipe_attn_fwd.  Returns (out, lse, o_saved or None)."""
+def layer_forward(cfg: Config, x, Wqkv, Wo, keep_o=False):
+    """Allocates out [L, D] bf16, lse [H, L] fp32 and runs the layer forward.
+    keep_o: False (O recomputed by the backward), True (O kept on the
+    device, upipe_attn_fwd's o_saved) or "host" (O kept in page-locked host
+    memory, upipe_attn_fwd_host_o).  Returns (out, lse, kept O or None)."""
     dev = x.device
     out = torch.empty((cfg.L, cfg.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((cfg.H, cfg.L), dtype=torch.float32, device=dev)
+    if keep_o == "host":
+        o_host = new_host_o(cfg)
+        attn_fwd_host_o(cfg, x, Wqkv, Wo, out, lse, o_host)
+        return out, lse, o_host
     o_saved = torch.empty((cfg.L, cfg.H * 128), dtype=torch.bfloat16, device=dev) if keep_o else None
     attn_fwd(cfg, x, Wqkv, Wo, out, lse, o_saved)
     return out, lse, o_saved
 
 
 def layer_backward(cfg: Config, x, Wqkv, Wo, dout, lse, o_saved=None):
-    """Allocates dx [L, D] bf16, dWqkv, dWo fp32 and runs upipe_attn_bwd."""
+    """Allocates dx [L, D] bf16, dWqkv, dWo fp32 and runs the layer backward
+    with the O that layer_forward kept (a host tensor selects
+    upipe_attn_bwd_host_o)."""
     dev = x.device
     dx = torch.empty((cfg.L, cfg.D), dtype=torch.bfloat16, device=dev)
     dWqkv = torch.empty(((cfg.H + 2 * cfg.Hkv) * 128, cfg.D), dtype=torch.float32, device=dev)
     dWo = torch.empty((cfg.D, cfg.H * 128), dtype=torch.float32, device=dev)
-    attn_bwd(cfg, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved)
+    if o_saved is not None and not o_saved.is_cuda:
+        attn_bwd_host_o(cfg, x, Wqkv, Wo, dout, lse, o_saved, dx, dWqkv, dWo)
+    else:
+        attn_bwd(cfg, x, Wqkv, Wo, dout, lse, dx, dWqkv, dWo, o_saved)
     return dx, dWqkv, dWo
 
 

@@ -109,12 +109,26 @@ typedef struct upipe_cfg {
   double rope_theta;
 } upipe_cfg;
 
+/* Where the layer entries keep the attention output O between the forward
+ * and the backward (the o_mode argument below):
+ *   UPIPE_O_RECOMPUTE  upipe_attn_fwd / _bwd with o_saved NULL: O lives in
+ *                      the workspace one chunk at a time; the backward
+ *                      recomputes it from the LSE
+ *   UPIPE_O_DEVICE     upipe_attn_fwd / _bwd with o_saved given
+ *   UPIPE_O_HOST       upipe_attn_fwd_host_o / _bwd_host_o: page-locked host
+ *                      memory holds it; two chunk buffers in the workspace  */
+#define UPIPE_O_RECOMPUTE 0
+#define UPIPE_O_DEVICE 1
+#define UPIPE_O_HOST 2
+
 /* Workspace bytes for one call.
  *   pass        0 = forward, 1 = backward
  *   core_only   1 = upipe_attn_core_fwd / _bwd, 0 = the layer entries
- *   has_o_saved 1 if the caller passes o_saved to the layer entries
- * Returns 0 for an invalid configuration (or a call that needs none).      */
-size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved);
+ *   o_mode      UPIPE_O_RECOMPUTE, UPIPE_O_DEVICE or UPIPE_O_HOST (layer
+ *               entries; ignored with core_only)
+ * Returns 0 for an invalid configuration, pass or o_mode (or a call that
+ * needs none).                                                             */
+size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int o_mode);
 
 /* Intermediate-activation accounting for one call (host arithmetic, no GPU):
  *   chunk_bytes  workspace that scales with U: the chunk's Q/K/V/O buffers
@@ -123,7 +137,7 @@ size_t upipe_workspace_bytes(const upipe_cfg* cfg, int pass, int core_only, int 
  *   fixed_bytes  workspace that does not scale with U: the fp32 output carry
  *                (out32 or dx32) and the RoPE table.
  * Returns UPIPE_OK or UPIPE_ERR_INVALID_ARG.                                */
-int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int has_o_saved,
+int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int o_mode,
                            size_t* chunk_bytes, size_t* fixed_bytes);
 
 /* Largest chunk size U whose workspace fits a memory budget.  The talk
@@ -134,13 +148,13 @@ int upipe_activation_bytes(const upipe_cfg* cfg, int pass, int core_only, int ha
  *   budget_bytes bytes the caller can give the workspace
  *   pass         0 = forward workspace, 1 = backward, 2 = the larger of the
  *                two (one workspace serving a whole training step)
- *   core_only, has_o_saved as for upipe_workspace_bytes
+ *   core_only, o_mode as for upipe_workspace_bytes
  * Considers every valid U (H % U == 0, and U % g == 0 or g % U == 0) and
  * returns the largest whose workspace is <= budget_bytes (the workspace is
  * not monotone in U: U = H drops the fp32 output carry).  Returns
  * UPIPE_ERR_INVALID_ARG for an invalid configuration or pass, and
  * UPIPE_ERR_WS_TOO_SMALL when no valid U fits.  Host arithmetic only.      */
-int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int has_o_saved);
+int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core_only, int o_mode);
 
 /* Layer forward (the write-up's paragraph on intermediate buffers).
  *   x        [L, D] bf16                 Wqkv [(H+2Hkv)*128, D] bf16
@@ -154,7 +168,8 @@ int upipe_choose_u(const upipe_cfg* cfg, size_t budget_bytes, int pass, int core
  *            same bits the backward's recomputation produces, so both
  *            backward variants return identical gradients; this costs the
  *            forward one more pass over the keys.
- *   ws       workspace of at least upipe_workspace_bytes(cfg, 0, 0, o_saved != NULL) */
+ *   ws       workspace of at least upipe_workspace_bytes(cfg, 0, 0, o_saved ?
+ *            UPIPE_O_DEVICE : UPIPE_O_RECOMPUTE)                          */
 int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
                    uint16_t* out, float* lse, uint16_t* o_saved, void* ws, size_t ws_bytes, void* stream);
 
@@ -164,10 +179,44 @@ int upipe_attn_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
  *   dx       [L, D] bf16 (written)
  *   dWqkv    [(H+2Hkv)*128, D] fp32 (written, not accumulated)
  *   dWo      [D, H*128] fp32 (written, not accumulated)
- *   ws       workspace of at least upipe_workspace_bytes(cfg, 1, 0, o_saved != NULL) */
+ *   ws       workspace of at least upipe_workspace_bytes(cfg, 1, 0, o_saved ?
+ *            UPIPE_O_DEVICE : UPIPE_O_RECOMPUTE)                          */
 int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
                    const uint16_t* dout, const float* lse, const uint16_t* o_saved, uint16_t* dx, float* dWqkv,
                    float* dWo, void* ws, size_t ws_bytes, void* stream);
+
+/* Layer forward and backward with O kept in host memory: the talk
+ * write-up's activation offloading (block activations that are expensive to
+ * recompute go to CPU memory and are prefetched for the backward pass)
+ * applied to the attention output, which the recomputing backward otherwise
+ * rebuilds with a second pass over the keys.  Device memory still scales
+ * with U: the workspace holds two chunk buffers of O, so that one chunk's
+ * copy runs while the next chunk computes.
+ *   o_host  L*H*128 bf16 (L*H*256 bytes) of page-locked host memory
+ *           (cudaHostAlloc, or cudaHostRegister'ed); chunk c's O_c [L, U*128]
+ *           sits at element offset c*L*U*128, so the layout depends on U and
+ *           the backward must use the forward's cfg.  Not page-locked, or
+ *           NULL: UPIPE_ERR_INVALID_ARG.
+ *   upipe_attn_fwd_host_o writes out and lse as upipe_attn_fwd does; O_c is
+ *     the online softmax's own output (not recomputed from the LSE), copied
+ *     to o_host on the library's device-to-host copy stream while the next
+ *     chunk runs.  Work enqueued on `stream` after the call sees o_host
+ *     complete.
+ *   upipe_attn_bwd_host_o returns the gradients of upipe_attn_bwd, with
+ *     O_c brought back on the host-to-device copy stream during chunk
+ *     c - 1 in place of the recomputation.  The gradients agree with the
+ *     recomputing backward's within rounding (O from the online softmax
+ *     differs from O recomputed from the LSE in its last bits), not bit for
+ *     bit.
+ *   ws  workspace of at least upipe_workspace_bytes(cfg, pass, 0,
+ *       UPIPE_O_HOST).
+ * Both hold the library's copy-stream lock for the duration of the host
+ * call (calls from several threads serialise their enqueueing).            */
+int upipe_attn_fwd_host_o(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                          uint16_t* out, float* lse, uint16_t* o_host, void* ws, size_t ws_bytes, void* stream);
+int upipe_attn_bwd_host_o(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, const uint16_t* Wo,
+                          const uint16_t* dout, const float* lse, const uint16_t* o_host, uint16_t* dx, float* dWqkv,
+                          float* dWo, void* ws, size_t ws_bytes, void* stream);
 
 /* Attention core only (no projection, no RoPE), the per-rank slice that
  * head-sharded context parallelism leaves on one GPU ("Untied Ulysses Pushes

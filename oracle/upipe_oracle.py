@@ -314,12 +314,16 @@ def layer_fwd(x, Wqkv, Wo, H, Hkv, theta, d=None, bf16_operands=False):
     return out, lse, o
 
 
-def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_operands=False):
+def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_operands=False, kept_o=False):
     """dx [L, D], dWqkv [(H+2Hkv)d, D], dWo [D, H d]: gradient of sum(out*dout).
 
     With ``bf16_operands`` every contraction input is rounded to bf16 (see
     the module header); the rounding itself is treated as the identity in
-    the chain rule.
+    the chain rule.  ``kept_o`` selects the O the backward reads under that
+    model: False, O recomputed from the forward's LSE (P enters P V as
+    bf16); True, the forward's own output kept from the forward pass (its
+    P V keeps P exact, as in layer_fwd).  Without ``bf16_operands`` the two
+    are the same exact O.
     """
     x = np.asarray(x, dtype=F64)
     Wqkv = np.asarray(Wqkv, dtype=F64)
@@ -331,8 +335,8 @@ def layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, d=None, bf16_operands=False):
     q, k, v = project_qkv(x, Wqkv, H, Hkv, d, theta)
     q, k, v = _op(q, bf16_operands), _op(k, bf16_operands), _op(v, bf16_operands)
     # O recomputed from the forward's LSE (P = exp(S - LSE), bf16 in P V
-    # under the precision model).
-    o, lse = attention_core_fwd(q, k, v, p_bf16=bf16_operands)
+    # under the precision model), or the forward's kept output.
+    o, lse = attention_core_fwd(q, k, v, p_bf16=bf16_operands and not kept_o)
     o = _op(o, bf16_operands)
     o_flat = o.reshape(L, H * d)
     dWo = dout.T @ o_flat

@@ -103,11 +103,15 @@ def test_workspace_arithmetic(lib):
     kvc = 1
     fwd = al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(L * D * 4)
     assert upipe.workspace_bytes(c, 0) == fwd
-    assert upipe.workspace_bytes(c, 0, has_o_saved=True) == fwd - al(U * slot)
+    assert upipe.workspace_bytes(c, 0, o_mode=upipe.O_DEVICE) == fwd - al(U * slot)
+    # O in host memory: two chunk buffers of O in place of one
+    assert upipe.workspace_bytes(c, 0, o_mode=upipe.O_HOST) == fwd - al(U * slot) + al(2 * U * slot)
+    assert upipe.workspace_bytes(c, 0, o_mode=3) == 0 and upipe.workspace_bytes(c, 0, o_mode=-1) == 0
     rec = U * ((L + 63) // 64) * 128 * 4  # LSE/Delta records
     bwd = (al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(U * slot) + al(rec)
            + al(2 * (U + 2 * kvc) * slot) + al(2 * L * 128 * 4) + al(L * D * 4))
     assert upipe.workspace_bytes(c, 1) == bwd
+    assert upipe.workspace_bytes(c, 1, o_mode=upipe.O_HOST) == bwd - al(U * slot) + al(2 * U * slot)
     # unchunked: no carries
     assert upipe.workspace_bytes(_cfg(U=8), 0) == al(L * 64 * 8) + al(12 * slot) + al(8 * slot)
     assert upipe.workspace_bytes(_cfg(), 0, core_only=True) == 0
@@ -235,3 +239,27 @@ def test_offload_entry_points_reject_null_buffers_before_any_copy(lib):
     assert lib.upipe_prefetch_async(None, None, 0, None) == upipe.UPIPE_OK
     assert lib.upipe_prefetch_async(None, ctypes.c_void_p(1 << 20), 64, None) == upipe.UPIPE_ERR_INVALID_ARG
     assert lib.upipe_offload_async(ctypes.c_void_p(1 << 20), None, 64, None) == upipe.UPIPE_ERR_INVALID_ARG
+
+
+def test_host_o_entry_points_reject_null_or_unpinned_buffers(lib):
+    """O kept in host memory must be page-locked: a null o_host is an
+    argument error in the library, a pageable or mis-sized tensor in the
+    binding; nothing is launched."""
+    import torch
+    c = _cfg().c()
+    fake = ctypes.c_void_p(1 << 20)
+    n0 = upipe.launch_count()
+    assert lib.upipe_attn_fwd_host_o(ctypes.byref(c), fake, fake, fake, fake, fake, None, fake, 1 << 30,
+                                     None) == upipe.UPIPE_ERR_INVALID_ARG
+    assert lib.upipe_attn_bwd_host_o(ctypes.byref(c), fake, fake, fake, fake, fake, None, fake, fake, fake, fake,
+                                     1 << 30, None) == upipe.UPIPE_ERR_INVALID_ARG
+    cfg = upipe.Config(L=256, D=256, H=4, Hkv=2, U=2)
+    x = torch.zeros(256, 256, dtype=torch.bfloat16)
+    w = torch.zeros(8 * 128, 256, dtype=torch.bfloat16)
+    wo = torch.zeros(256, 512, dtype=torch.bfloat16)
+    lse = torch.zeros(4, 256)
+    with pytest.raises(ValueError, match="o_host"):
+        upipe.attn_fwd_host_o(cfg, x, w, wo, x, lse, torch.zeros(256 * 512, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="o_host"):
+        upipe.attn_fwd_host_o(cfg, x, w, wo, x, lse, torch.zeros(7, dtype=torch.bfloat16))
+    assert upipe.launch_count() == n0

@@ -87,7 +87,7 @@ def _nbytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts)
 
 
-def _run_layer(shape, U, inputs, on_device=None, peaks=None):
+def _run_layer(shape, U, inputs, on_device=None, peaks=None, keep_o=False):
     """Full-size forward + backward.  Returns the five results on the host,
     or on the device when `on_device` (then the device inputs too).  With a
     dict `peaks`, records the device high-water mark of each pass's
@@ -99,12 +99,12 @@ def _run_layer(shape, U, inputs, on_device=None, peaks=None):
     torch.cuda.synchronize()
     base = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
-    out, lse, _ = upipe.layer_forward(cfg, xd, wd, wod)
+    out, lse, kept = upipe.layer_forward(cfg, xd, wd, wod, keep_o=keep_o)
     torch.cuda.synchronize()
     fwd_peak = torch.cuda.max_memory_allocated() - base - _nbytes(out, lse)
     base = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
-    dx, dwqkv, dwo = upipe.layer_backward(cfg, xd, wd, wod, dd, lse)
+    dx, dwqkv, dwo = upipe.layer_backward(cfg, xd, wd, wod, dd, lse, kept)
     torch.cuda.synchronize()
     bwd_peak = torch.cuda.max_memory_allocated() - base - _nbytes(dx, dwqkv, dwo)
     status_ok()
@@ -129,11 +129,13 @@ def _fwd_rows(Q, K, V, rows, g, scale):
     return O, Lr
 
 
-def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
+def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta, kept_o=False):
     """dQ, dK, dV of the last T positions (RoPE undone on dQ, dK).  Heads are
     independent, so they run on a thread pool (NumPy releases the GIL in its
     matrix products and element-wise loops); each head's dK/dV share is
-    summed into its KV head afterwards, in head order."""
+    summed into its KV head afterwards, in head order.  kept_o: the backward
+    reads the forward's own O (P exact in P V) instead of O recomputed from
+    the LSE."""
     T, H = Qt.shape[0], Qt.shape[1]
     Hkv = K.shape[1]
     rnd = orc.bf16_round if bf else (lambda a: a)
@@ -143,8 +145,8 @@ def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
 
     def head(h):
         kh, vh = K[:, h // g], V[:, h // g]
-        # O recomputed from the LSE, as the backward does
-        o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, p_bf16=bf)
+        # O recomputed from the LSE, as the backward does (or the kept one)
+        o_t, l_t = orc.attention_head_rows(Qt[:, h], tpos, kh, vh, scale, p_bf16=bf and not kept_o)
         o_t = rnd(o_t)
         dq_h = orc.attention_dq_rows(Qt[:, h], tpos, kh, vh, dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
         a, b = orc.attention_dkv_tail(Qt[:, h], kh[tpos], vh[tpos], dOt[:, h], o_t, l_t, scale, bf16_operands=bf)
@@ -161,10 +163,12 @@ def _tail(Qt, dOt, K, V, tpos, g, scale, bf, theta):
     return np.concatenate([dq.reshape(T, -1), dk.reshape(T, -1), dv.reshape(T, -1)], 1)
 
 
-def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=False):
+def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=False, kept_o=False, kv=None):
     """Sampled forward rows, the backward tail and one head's dWo columns
     against the precision-model oracle (and, with `plain`, against the plain
-    fp64 definition as well)."""
+    fp64 definition as well).  kept_o: the backward read the forward's own
+    O (O kept in host memory).  kv: (K, V, Kb, Vb) of an earlier call on the
+    same inputs."""
     x, w, wo, dout = inputs
     out, lse, dx, dwqkv, dwo = res
     H, Hkv, L = shape.H, shape.Hkv, shape.L
@@ -174,7 +178,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
     uni, edge = fwd_rows
     fwd_rows = np.unique(np.concatenate([uni, edge]))
     need = L if (tail or dwo_head is not None) else int(fwd_rows.max()) + 1
-    K, V, Kb, Vb = _kv_all(x, w, shape, need, exact=plain)
+    K, V, Kb, Vb = kv if kv is not None else _kv_all(x, w, shape, need, exact=plain)
     Wo = wo.to(torch.float64).numpy()
     W = w.to(torch.float64).numpy()
     iu = np.searchsorted(fwd_rows, uni)
@@ -200,7 +204,7 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
         tpos = np.arange(L - T, L)
         Qt = _proj_rows(x, w, wq_rows, tpos, shape.theta, True)
         dOt = (dout[tpos].to(torch.float64).numpy() @ Wo).reshape(T, H, D_HEAD)
-        dqkv = _tail(orc.bf16_round(Qt), orc.bf16_round(dOt), Kb, Vb, tpos, g, scale, True, shape.theta)
+        dqkv = _tail(orc.bf16_round(Qt), orc.bf16_round(dOt), Kb, Vb, tpos, g, scale, True, shape.theta, kept_o)
         got = f64(dx[tpos])
         assert_close(got, dqkv @ W, "dx tail rows")
         if plain:
@@ -215,10 +219,10 @@ def _check_layer_rows(shape, inputs, res, fwd_rows, tail, dwo_head=None, plain=F
             pos = allpos[s0:s0 + 16384]
             Qh[pos] = _proj_rows(x, w, np.arange(h * D_HEAD, (h + 1) * D_HEAD), pos, shape.theta, True)[:, 0]
         Oh, _ = orc.attention_head_rows(orc.bf16_round(Qh), allpos, Kb[:, h // g], Vb[:, h // g], scale,
-                                        p_bf16=True)  # the backward's O, recomputed from the LSE
+                                        p_bf16=not kept_o)  # the backward's O: recomputed from the LSE, or kept
         ref = dout.to(torch.float64).numpy().T @ orc.bf16_round(Oh)
         assert_close(f64(dwo[:, h * D_HEAD:(h + 1) * D_HEAD]), ref, "dWo head columns", weight_grad=True)
-    return Kb, Vb
+    return K, V, Kb, Vb
 
 
 def _check_dwqkv_group(shape, inputs, dwqkv, kv, Kb, Vb):
@@ -269,7 +273,7 @@ def test_llama3_8b_layer_L32768():
     shape = synth.LLAMA8B
     inputs = synth.layer_inputs(shape)
     res = _run_layer(shape, 8, inputs)
-    Kb, Vb = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
+    _, _, Kb, Vb = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
     _check_dwqkv_group(shape, inputs, res[3], 1, Kb, Vb)
     _assert_bit_exact(res, _run_layer(shape, 32, inputs), "U=8 vs U=32")
 
@@ -284,7 +288,13 @@ def test_qwen32b_shape_layer_L131072_u_sweep():
     inputs = synth.layer_inputs(shape)
     peaks = {}
     res8 = _run_layer(shape, 8, inputs, peaks=peaks)
-    _check_layer_rows(shape, inputs, res8, _rows(shape.L, n=6), tail=128)
+    kv = _check_layer_rows(shape, inputs, res8, _rows(shape.L, n=6), tail=128)
+    # O kept in page-locked host memory (the benchmark's mode): eight chunks
+    # through the two staging buffers; the forward is the recomputing
+    # forward's bit for bit, the backward is checked against the kept-O model.
+    res_h = _run_layer(shape, 8, inputs, keep_o="host")
+    assert torch.equal(res_h[0], res8[0]) and torch.equal(res_h[1], res8[1])
+    _check_layer_rows(shape, inputs, res_h, _rows(shape.L, n=6), tail=128, dwo_head=9, kept_o=True, kv=kv)
     for U in (16, 64):
         _assert_bit_exact(res8, _run_layer(shape, U, inputs, peaks=peaks), f"U=8 vs U={U}")
     chunk = {}
@@ -447,3 +457,4 @@ def test_ulysses_slice_core_L1M():
         dv_t += b
     assert_close(f64(dk[tpos, 0]), dk_t, "dk tail")
     assert_close(f64(dv[tpos, 0]), dv_t, "dv tail")
+

@@ -38,14 +38,14 @@ def _run(shape, U, keep_o=False):
     return (x, wqkv, wo, dout), (out, lse, dx, dwqkv, dwo)
 
 
-def _check_vs_oracle(shape, inputs, outs):
+def _check_vs_oracle(shape, inputs, outs, kept_o=False):
     x, wqkv, wo, dout = (f64(t) for t in inputs)
     got = [f64(t) for t in outs]
     names = ("out", "lse", "dx", "dWqkv", "dWo")
     wgrad = (False, False, False, True, True)
     args = (x, wqkv, wo, shape.H, shape.Hkv, shape.theta)
     m_out, m_lse, _ = orc.layer_fwd(*args, bf16_operands=True)
-    m_bwd = orc.layer_bwd(x, wqkv, wo, dout, shape.H, shape.Hkv, shape.theta, bf16_operands=True)
+    m_bwd = orc.layer_bwd(x, wqkv, wo, dout, shape.H, shape.Hkv, shape.theta, bf16_operands=True, kept_o=kept_o)
     model = (m_out, m_lse, *m_bwd)
     for g_, m, n, wg in zip(got, model, names, wgrad):
         assert_close(g_, m, n, weight_grad=wg)
@@ -94,3 +94,28 @@ def test_saved_o_matches_recompute():
         assert torch.equal(x, y), n
     assert_close(f64(a[0]), f64(b[0]), "out (online softmax) vs out (kept O)")
     _check_vs_oracle(shape, inputs, b)
+
+
+@pytest.mark.parametrize("L,D,H,Hkv,U", [(1024, 1024, 8, 2, 2), (300, 256, 4, 2, 4), (129, 128, 4, 1, 1),
+                                         (65, 256, 8, 2, 1)])
+def test_host_o_matches_oracle(L, D, H, Hkv, U):
+    """O kept in page-locked host memory (one and several chunks; with four
+    and more chunks both staging buffers are reused).  The forward is the
+    recomputing forward's bit for bit; the backward reads the forward's own
+    O, which the oracle's kept-O model describes (the two backward modes
+    differ by the bf16 rounding of two different O, the precision model's
+    own deviation, so each is checked against its own model)."""
+    shape = synth.LayerShape(L=L, D=D, H=H, Hkv=Hkv, U=U)
+    inputs, h = _run(shape, U, keep_o="host")
+    _, r = _run(shape, U)
+    assert torch.equal(h[0], r[0]) and torch.equal(h[1], r[1]), "forward differs from the recomputing forward"
+    _check_vs_oracle(shape, inputs, h, kept_o=True)
+
+
+def test_host_o_every_chunk_size_is_bit_exact_to_unchunked():
+    shape = synth.LayerShape(L=333, D=256, H=8, Hkv=4)
+    _, ref = _run(shape, 8, keep_o="host")
+    for U in (1, 2, 4):
+        _, outs = _run(shape, U, keep_o="host")
+        for a, b, n in zip(ref, outs, ("out", "lse", "dx", "dWqkv", "dWo")):
+            assert torch.equal(a, b), f"U={U}: {n} differs from the unchunked run"

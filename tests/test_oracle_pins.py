@@ -368,7 +368,6 @@ def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs()
     q, k, v = (_bf(t) for t in orc.project_qkv(x, Wqkv, H, Hkv, d, theta))
     o = np.zeros((L, H, d))
     lse = np.zeros((H, L))
-    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     causal = np.tril(np.ones((L, L), dtype=bool))
     o_fwd = np.zeros((L, H, d))
     for h in range(H):
@@ -381,23 +380,35 @@ def test_bf16_operand_layer_is_the_exact_layer_with_rounded_contraction_inputs()
     o_fwd = _bf(o_fwd)
     o = _bf(o)
     do = _bf((dout @ Wo).reshape(L, H, d))
-    for h in range(H):
-        S = q[:, h] @ k[:, h // g].T * sc
-        P = np.where(causal, np.exp(S - lse[h][:, None]), 0.0)
-        delta = np.sum(do[:, h] * o[:, h], axis=1)
-        dS = _bf(P * (do[:, h] @ v[:, h // g].T - delta[:, None]))
-        dv[:, h // g] += _bf(P).T @ do[:, h]
-        dk[:, h // g] += dS.T @ q[:, h] * sc
-        dq[:, h] = dS @ k[:, h // g] * sc
+    pos = np.arange(L)
+
+    def grads(o_used):
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for h in range(H):
+            S = q[:, h] @ k[:, h // g].T * sc
+            P = np.where(causal, np.exp(S - lse[h][:, None]), 0.0)
+            delta = np.sum(do[:, h] * o_used[:, h], axis=1)
+            dS = _bf(P * (do[:, h] @ v[:, h // g].T - delta[:, None]))
+            dv[:, h // g] += _bf(P).T @ do[:, h]
+            dk[:, h // g] += dS.T @ q[:, h] * sc
+            dq[:, h] = dS @ k[:, h // g] * sc
+        dqkv = np.concatenate([orc.rope_apply(dq, pos, theta, inverse=True).reshape(L, -1),
+                               orc.rope_apply(dk, pos, theta, inverse=True).reshape(L, -1), dv.reshape(L, -1)], 1)
+        return dqkv @ Wqkv, dqkv.T @ x, dout.T @ o_used.reshape(L, -1)
+
     np.testing.assert_allclose(lse_b, lse, atol=1e-13)
     np.testing.assert_allclose(o_b, o_fwd, atol=1e-13)
     np.testing.assert_allclose(out_b, o_fwd.reshape(L, -1) @ Wo.T, atol=1e-13)
-    pos = np.arange(L)
-    dqkv = np.concatenate([orc.rope_apply(dq, pos, theta, inverse=True).reshape(L, -1),
-                           orc.rope_apply(dk, pos, theta, inverse=True).reshape(L, -1), dv.reshape(L, -1)], 1)
-    np.testing.assert_allclose(dx_b, dqkv @ Wqkv, atol=1e-12)
-    np.testing.assert_allclose(dW_b, dqkv.T @ x, atol=1e-12)
-    np.testing.assert_allclose(dWo_b, dout.T @ o.reshape(L, -1), atol=1e-12)
+    for got, ref in zip((dx_b, dW_b, dWo_b), grads(o)):
+        np.testing.assert_allclose(got, ref, atol=1e-12)
+    # O kept from the forward: the backward reads the forward's own output
+    kept = orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, bf16_operands=True, kept_o=True)
+    for got, ref in zip(kept, grads(o_fwd)):
+        np.testing.assert_allclose(got, ref, atol=1e-12)
+    assert np.abs(kept[2] - dWo_b).max() > 0  # the two O differ at the bf16 level
+    for a_, b_ in zip(orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta, kept_o=True),
+                      orc.layer_bwd(x, Wqkv, Wo, dout, H, Hkv, theta)):
+        np.testing.assert_array_equal(a_, b_)  # without the model both are the exact O
     out, _, _ = orc.layer_fwd(x, Wqkv, Wo, H, Hkv, theta)
     rel = np.linalg.norm(out_b - out) / np.linalg.norm(out)
     assert 1e-5 < rel < 1e-2
