@@ -6,7 +6,7 @@ and rounded once to bf16; the oracle receives the same bf16 values (upcast
 to fp64), the CUDA path receives them as bf16.
 
 Seeds: x=0, Wqkv=1, Wo=2, dout=3 (layer inputs); q=0, k=1, v=2, dO=3 (core
-inputs).  Distributions: activations and upstream gradients ~ N(0, 1),
+inputs); 10..13 (MLP inputs), 20..22 (loss inputs).  Distributions: activations and upstream gradients ~ N(0, 1),
 weights ~ N(0, 0.02).
 """
 
@@ -64,6 +64,30 @@ def core_inputs(L: int, H: int, Hkv: int, d: int = 128, device="cpu"):
     v = _randn((L, Hkv, d), 2, 1.0, device)
     do = _randn((L, H, d), 3, 1.0, device)
     return q, k, v, do
+
+
+def mlp_inputs(L: int, D: int, F: int, device="cpu", w_std=0.02):
+    """x [L, D], Wgu [2F, D] (gate rows, then up rows), Wd [D, F], dy [L, D],
+    all bf16 (seeds 10..13)."""
+    x = _randn((L, D), 10, 1.0, device)
+    wgu = _randn((2 * F, D), 11, w_std, device)
+    wd = _randn((D, F), 12, w_std, device)
+    dy = _randn((L, D), 13, 1.0, device)
+    return x, wgu, wd, dy
+
+
+def ce_inputs(L: int, D: int, V: int, device="cpu", w_std=0.02, ignore_every=17):
+    """h [L, D], W [V, D] bf16 (seeds 20, 21) and int32 labels [L] uniform
+    over the vocabulary (seed 22), every `ignore_every`-th one set to -100
+    (ignored)."""
+    h = _randn((L, D), 20, 1.0, device)
+    w = _randn((V, D), 21, w_std, device)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(22)
+    labels = torch.randint(0, V, (L,), generator=g, dtype=torch.int32)
+    if ignore_every:
+        labels[ignore_every - 1::ignore_every] = -100
+    return h, w, labels.to(device)
 
 
 # The five workloads, by name.
