@@ -63,7 +63,8 @@ constexpr int kTile = 128 * 64 * 2;  // one 16 KB operand tile (128 x 64 bf16)
 template <int KIND>
 struct Layout {
   static constexpr bool kSplit = (KIND == GK_DWQKV || KIND == GK_DX);
-  static constexpr int kStages = kSplit ? 4 : (KIND == GK_OPROJ ? 5 : 6);
+  static constexpr bool kCarryKind = (KIND == GK_OPROJ || KIND == GK_DX || KIND == GK_WGRAD);
+  static constexpr int kStages = kSplit ? 4 : (kCarryKind ? 5 : 6);
   static constexpr int kA = kSplit ? 2 * kTile : kTile;
   static constexpr int kB = kTile;  // this CTA's 128-column slot of the pair's 256
   static constexpr int kStage = kA + kB;
@@ -72,8 +73,7 @@ struct Layout {
   // accesses are whole 128-byte lines.  The O projection (K = U d, short
   // products) stages a whole 128-column slot so that its carry loads are in
   // flight together; dx hides one chunk at a time behind its longer products.
-  static constexpr bool kCarryKind = (KIND == GK_OPROJ || KIND == GK_DX);
-  static constexpr int kXposeChunks = KIND == GK_OPROJ ? 4 : 1;
+  static constexpr int kXposeChunks = KIND == GK_DX ? 1 : 4;
   static constexpr int OFF_XPOSE = kStages * kStage;
   static constexpr int OFF_BAR = OFF_XPOSE + (kCarryKind ? 4 * kXposeChunks * 4096 : 0);
   static constexpr int B_FULL = 0;                    // even CTA: both CTAs' copies of the stage landed
@@ -98,16 +98,20 @@ template <> struct Traits<GK_DO>    { static constexpr int a_mn = 0, b_mn = 1; }
 template <> struct Traits<GK_DWO>   { static constexpr int a_mn = 1, b_mn = 1; };
 template <> struct Traits<GK_DWQKV> { static constexpr int a_mn = 1, b_mn = 1; };
 template <> struct Traits<GK_DX>    { static constexpr int a_mn = 0, b_mn = 1; };
+template <> struct Traits<GK_GU>    { static constexpr int a_mn = 0, b_mn = 0; };
+template <> struct Traits<GK_GU_BWD> { static constexpr int a_mn = 0, b_mn = 0; };
+template <> struct Traits<GK_NN>    { static constexpr int a_mn = 0, b_mn = 1; };
+template <> struct Traits<GK_WGRAD> { static constexpr int a_mn = 1, b_mn = 1; };
 
 // `bar` is the shared::cluster address of the even CTA's stage barrier.
 template <int KIND>
 __device__ __forceinline__ void load_a(const CUtensorMap* m, const GemmParams& p, uint32_t dst, uint32_t bar,
                                        int mt, int kb) {
-  if constexpr (KIND == GK_QKV || KIND == GK_DO) {
+  if constexpr (KIND == GK_QKV || KIND == GK_DO || KIND == GK_GU || KIND == GK_GU_BWD || KIND == GK_NN) {
     tma_load_2d_pair(dst, m, bar, kb * 64, mt * 128);
   } else if constexpr (KIND == GK_OPROJ) {
     tma_load_2d_pair(dst, m, bar, p.a_col0 + kb * 64, mt * 128);
-  } else if constexpr (KIND == GK_DWO) {
+  } else if constexpr (KIND == GK_DWO || KIND == GK_WGRAD) {
     tma_load_2d_pair(dst, m, bar, mt * 128, kb * 64);
     tma_load_2d_pair(dst + 8192, m, bar, mt * 128 + 64, kb * 64);
   } else if constexpr (KIND == GK_DWQKV) {
@@ -130,7 +134,11 @@ __device__ __forceinline__ void load_b(const CUtensorMap* m, const GemmParams& p
     tma_load_2d_pair(dst, m, bar, kb * 64, p.tab0[nt] * 128);
   } else if constexpr (KIND == GK_OPROJ) {
     tma_load_2d_pair(dst, m, bar, p.b_col0 + kb * 64, nt * 128);
-  } else if constexpr (KIND == GK_DO || KIND == GK_DWO || KIND == GK_DWQKV) {
+  } else if constexpr (KIND == GK_GU || KIND == GK_GU_BWD) {
+    // B slot 2 np holds gate rows np*128.., slot 2 np + 1 the up rows
+    // F + np*128..: each CTA of the pair ends with [g | u] of one f range.
+    tma_load_2d_pair(dst, m, bar, kb * 64, ((nt & 1) ? p.b_col0 : 0) + (nt >> 1) * 128);
+  } else if constexpr (KIND == GK_DO || KIND == GK_DWO || KIND == GK_DWQKV || KIND == GK_NN || KIND == GK_WGRAD) {
     tma_load_2d_pair(dst, m, bar, p.b_col0 + nt * 128, kb * 64);
     tma_load_2d_pair(dst + 8192, m, bar, p.b_col0 + nt * 128 + 64, kb * 64);
   } else {  // GK_DX
@@ -219,7 +227,7 @@ __device__ __forceinline__ void carry_row32(uint32_t xs, uint32_t (&v)[32]) {
 template <int KIND>
 __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, int m, int r, int mt, int nt,
                                            bool valid, uint32_t xs) {
-  constexpr bool kCarry = (KIND == GK_OPROJ || KIND == GK_DX);
+  constexpr bool kCarry = Layout<KIND>::kCarryKind;
   if constexpr (KIND == GK_QKV) {
     const int slot = nt;
     __nv_bfloat16* orow =
@@ -305,6 +313,8 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
         frow = p.carry + static_cast<int64_t>(m) * p.N + nt * 128;
     } else if constexpr (KIND == GK_DWO) {
       frow = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ld_out + p.out_col0 + nt * 128;
+    } else if constexpr (KIND == GK_NN) {
+      brow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(m) * p.ld_out + nt * 128;
     } else {  // GK_DWQKV
       frow = static_cast<float*>(p.out) + static_cast<int64_t>(p.tab1[mt] * 128 + r) * p.ld_out + nt * 128;
     }
@@ -352,6 +362,74 @@ __device__ __forceinline__ void store_slot(const GemmParams& p, uint32_t trow, i
   }
 }
 
+// SwiGLU epilogue of the gate/up GEMM: accumulator columns [0, 128) hold
+// g = x Wg^T and [128, 256) u = x Wu^T for features f = 128 np + c of row m.
+// Forward: H = silu(g) u.  Backward (dH from in2): H, dG = dH u silu'(g) and
+// dU = dH silu(g), with s = sigmoid(g), silu = g s, silu' = s (1 + g (1 - s)).
+template <int KIND>
+__device__ __forceinline__ void store_gu(const GemmParams& p, uint32_t tacc, int m, int np, bool valid) {
+  const int64_t f0 = static_cast<int64_t>(np) * 128;
+  __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(m) * p.ld_out + f0;
+#pragma unroll 1
+  for (int c4 = 0; c4 < 4; ++c4) {
+    uint32_t g[32], u[32];
+    tmem_ld32(tacc + c4 * 32, g);
+    tmem_ld32(tacc + 128 + c4 * 32, u);
+    tmem_ld_wait(g);
+    tmem_ld_wait(u);
+    if (!valid) continue;
+    float dh[32];
+    if constexpr (KIND == GK_GU_BWD) {
+      const __nv_bfloat16* drow = p.in2 + static_cast<int64_t>(m) * p.ld_in2 + f0 + c4 * 32;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ld_global_nc_v4(drow + q * 8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dh[8 * q + 2 * e] = bf16_lo(w[e]);
+          dh[8 * q + 2 * e + 1] = bf16_hi(w[e]);
+        }
+      }
+    }
+    uint32_t hp[16], dgp[16], dup[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float hv[2], dg[2], du[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float gv = __uint_as_float(g[2 * i + e]);
+        const float uv = __uint_as_float(u[2 * i + e]);
+        const float sg = 1.0f / (1.0f + __expf(-gv));
+        const float silu = gv * sg;
+        hv[e] = silu * uv;
+        if constexpr (KIND == GK_GU_BWD) {
+          const float d = dh[2 * i + e];
+          dg[e] = d * uv * (sg * (1.0f + gv * (1.0f - sg)));
+          du[e] = d * silu;
+        }
+      }
+      hp[i] = pack_bf16x2(hv[0], hv[1]);
+      if constexpr (KIND == GK_GU_BWD) {
+        dgp[i] = pack_bf16x2(dg[0], dg[1]);
+        dup[i] = pack_bf16x2(du[0], du[1]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_global_v4(hrow + c4 * 32 + q * 8, hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+    if constexpr (KIND == GK_GU_BWD) {
+      __nv_bfloat16* grow = p.out2 + static_cast<int64_t>(m) * p.ld_out2 + f0 + c4 * 32;
+      __nv_bfloat16* urow = grow + p.b_col0;  // dU block starts at column F
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        st_global_v4(grow + q * 8, dgp[4 * q], dgp[4 * q + 1], dgp[4 * q + 2], dgp[4 * q + 3]);
+        st_global_v4(urow + q * 8, dup[4 * q], dup[4 * q + 1], dup[4 * q + 2], dup[4 * q + 3]);
+      }
+    }
+  }
+}
+
 template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
@@ -383,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lt::OFF_ABORT);
   const WaitCtl w{abort_flag, p.status, p.limit_ns};
-  constexpr bool kCarry = (KIND == GK_OPROJ || KIND == GK_DX);
+  constexpr bool kCarry = Lt::kCarryKind;
   const bool carry_in = kCarry && p.carry_in;
 
   if (threadIdx.x == 0) {
@@ -544,9 +622,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait<true>(bar(B_ACC_FULL + b), (i >> 1) & 1, w))) break;
       tc_fence_after();
       if (tile_ok) {
-        for (int j = 0; j < nsl; ++j) {
-          const uint32_t trow = trow0 + b * 256 + j * 128;
-          store_slot<KIND>(p, trow, m, r, mt, nt0 + j, valid, xs);
+        if constexpr (KIND == GK_GU || KIND == GK_GU_BWD) {
+          store_gu<KIND>(p, trow0 + b * 256, m, tt % n_pairs, valid);
+        } else {
+          for (int j = 0; j < nsl; ++j) {
+            const uint32_t trow = trow0 + b * 256 + j * 128;
+            store_slot<KIND>(p, trow, m, r, mt, nt0 + j, valid, xs);
+          }
         }
       }
       if (t + 2 * G < total) prep(i + 2, t + 2 * G);
@@ -628,6 +710,10 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& a, const CUtensorMap& 
     case GK_DWO: return launch_kind<GK_DWO>(a, b, p, s);
     case GK_DWQKV: return launch_kind<GK_DWQKV>(a, b, p, s);
     case GK_DX: return launch_kind<GK_DX>(a, b, p, s);
+    case GK_GU: return launch_kind<GK_GU>(a, b, p, s);
+    case GK_GU_BWD: return launch_kind<GK_GU_BWD>(a, b, p, s);
+    case GK_NN: return launch_kind<GK_NN>(a, b, p, s);
+    case GK_WGRAD: return launch_kind<GK_WGRAD>(a, b, p, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -19,6 +19,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "host.h"
 #include "upipe.h"
 #include "upipe_internal.h"
 
@@ -126,6 +127,10 @@ Plan make_plan(const Shape& s, int pass, bool core, int o_mode) {
   return p;
 }
 
+}  // namespace
+
+// ------------------------------------------- helpers shared through host.h
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 uint64_t spin_limit_ns() {
@@ -223,10 +228,6 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t heads, uint
 std::atomic<int64_t> g_launches{0};
 std::atomic<bool> g_profile{false};
 thread_local bool t_no_profile = false;
-struct ProfRec {
-  int kind;
-  cudaEvent_t a, b;
-};
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -241,31 +242,12 @@ cudaEvent_t pool_event() {
   return e;
 }
 
-}  // namespace
-
 // See upipe_internal.h.
 ProfilingOff::ProfilingOff() : prev_(t_no_profile) { t_no_profile = true; }
 ProfilingOff::~ProfilingOff() { t_no_profile = prev_; }
 
 namespace {
 
-template <class F>
-cudaError_t counted(int kind, cudaStream_t st, F&& launch) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (!g_profile.load(std::memory_order_relaxed) || t_no_profile) return launch();
-  ProfRec r{kind, pool_event(), pool_event()};
-  cudaEventRecord(r.a, st);
-  const cudaError_t e = launch();
-  cudaEventRecord(r.b, st);
-  g_prof.push_back(r);
-  return e;
-}
-
-#define UPIPE_CU(x)                          \
-  do {                                       \
-    if ((x) != cudaSuccess) return UPIPE_ERR_CUDA; \
-  } while (0)
-#define UPIPE_LAUNCH(kind, x) UPIPE_CU(counted(kind, st, [&] { return (x); }))
 // dQ and dK/dV of one chunk run concurrently: neither reads what the other
 // writes.  dK/dV goes to a second stream of the device's greatest priority,
 // so its CTAs (few, long: key tile kb sees L - 128 kb queries of g_loc
@@ -363,10 +345,6 @@ int async_copy(void* dst, const void* src, size_t bytes, bool to_host, cudaStrea
   return UPIPE_OK;
 }
 
-#define UPIPE_MAP(x)                                 \
-  do {                                               \
-    if (!(x)) return UPIPE_ERR_CUDA;                 \
-  } while (0)
 
 // Page-locked (or registered) host memory: the only kind a copy stream
 // copies without blocking the calling thread.
@@ -393,14 +371,6 @@ int copy_o_chunk(Copier* cp, void* dst, const void* src, size_t bytes, bool to_h
 }
 
 using bf16 = __nv_bfloat16;
-
-GemmParams gemm_base(int* status, uint64_t limit) {
-  GemmParams g;
-  std::memset(&g, 0, sizeof(g));
-  g.status = status;
-  g.limit_ns = limit;
-  return g;
-}
 
 // Chunk c: query heads [c*U, (c+1)*U); first KV head and W row blocks.
 struct Chunk {

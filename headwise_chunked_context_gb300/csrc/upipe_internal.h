@@ -20,9 +20,10 @@ constexpr int kMaxSlots = 96;     // H + 2 Hkv limit (per-slot tables below)
 // ------------------------------------------------------------------ GEMMs
 //
 // One tcgen05 GEMM kernel (persistent CTA pairs, 256x256 output tiles, K
-// blocks of 64) serves the six projection contractions of the layer.  The kind fixes which operands
-// are K-major or MN-major, how tile coordinates map to tensor coordinates
-// and what the epilogue does.
+// blocks of 64) serves the six projection contractions of the layer and the
+// contractions of the sequence-tiled MLP and loss.  The kind fixes which
+// operands are K-major or MN-major, how tile coordinates map to tensor
+// coordinates and what the epilogue does.
 enum GemmKind : int {
   GK_QKV = 0,    // Y_c = x W_c^T, fused RoPE + bf16 cast into head-major Q/K/V
   GK_OPROJ = 1,  // out32 (+)= O_c Wo[:, cols_c]^T with an fp32 carry
@@ -30,6 +31,12 @@ enum GemmKind : int {
   GK_DWO = 3,    // dWo[:, cols_c] = dout^T O_c (fp32)
   GK_DWQKV = 4,  // dWqkv[rows_c] = dqkv_c^T x (fp32)
   GK_DX = 5,     // dx32 (+)= dqkv_c W_c with an fp32 carry
+  // Sequence-tiled MLP and loss.  GK_OPROJ also serves them as a plain
+  // A B^T (both K-major): bf16 out (final_out) or fp32 out (no carry_in).
+  GK_GU = 6,      // H = silu(X Wg^T) * (X Wu^T) -> bf16 [M, F]; B = Wgu [2F, K], b_col0 = F
+  GK_GU_BWD = 7,  // from X Wgu^T and dH (in2): H -> out, [dG | dU] -> out2 (bf16 [M, 2F])
+  GK_NN = 8,      // C = A B, A [M, K] K-major, B [K, N] (N contiguous) -> bf16 [M, N]
+  GK_WGRAD = 9,   // C (+)= A^T B, A [K, M], B [K, N] (both M/N contiguous), fp32 C in `carry` [M, N]
 };
 
 struct GemmParams {
@@ -54,6 +61,10 @@ struct GemmParams {
   int lo_z;                    // DWQKV / DX: A slot offset of the low bf16 halves (0 = no split)
   int k_mid;                   // DWQKV: > 0 splits K into blocks [0, k_mid) and [k_mid, k_blocks), two
                                // work units per tile that add into the zeroed output (fp32 reductions)
+  const __nv_bfloat16* in2;    // GU_BWD: dH [M, F]
+  int64_t ld_in2;
+  __nv_bfloat16* out2;         // GU_BWD: [dG | dU] [M, 2F]
+  int64_t ld_out2;
   int* status;
   uint64_t limit_ns;
 };
@@ -145,5 +156,11 @@ cudaError_t launch_delta(const __nv_bfloat16* o, int64_t o_row, int64_t o_head, 
 // dimension ld) for the n row blocks b listed in `blocks`.
 cudaError_t launch_zero_rows(float* base, int64_t ld, int cols, const int16_t* blocks, int n, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
+// Cross-entropy rows: for each of the `rows` rows of the fp32 logits z
+// (leading dimension ld_z, V columns), LSE, the row's loss (0 for a negative
+// label) and dz = scale (softmax - onehot) as bf16 (leading dimension ld_dz;
+// a row of zeros for a negative label).
+cudaError_t launch_ce_rows(const float* z, int64_t ld_z, int V, const int32_t* labels, float scale, float* loss,
+                           __nv_bfloat16* dz, int64_t ld_dz, int rows, cudaStream_t s);
 
 }  // namespace upipe

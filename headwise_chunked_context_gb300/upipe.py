@@ -39,6 +39,11 @@ EXPORTS = (
     "upipe_attn_core_fwd",
     "upipe_attn_core_bwd",
     "upipe_attn_core_bwd_noalloc",
+    "upipe_mlp_workspace_bytes",
+    "upipe_mlp_fwd",
+    "upipe_mlp_bwd",
+    "upipe_ce_workspace_bytes",
+    "upipe_ce_fwd_bwd",
     "upipe_offload_async",
     "upipe_prefetch_async",
     "upipe_copies_join",
@@ -51,7 +56,8 @@ EXPORTS = (
 )
 
 KINDS = ("rope_table", "qkv_gemm", "attn_fwd", "oproj_gemm", "do_gemm", "dwo_gemm", "attn_bwd_dq",
-         "attn_bwd_dkdv", "dwqkv_gemm", "dx_gemm", "delta", "zero_rows")
+         "attn_bwd_dkdv", "dwqkv_gemm", "dx_gemm", "delta", "zero_rows", "alst_gu", "alst_gemm", "alst_wgrad",
+         "ce_rows")
 
 
 class UpipeError(RuntimeError):
@@ -73,6 +79,18 @@ class Cfg(ctypes.Structure):
         ("causal", ctypes.c_int32),
         ("rope_theta", ctypes.c_double),
     ]
+
+
+class MlpCfg(ctypes.Structure):
+    """Mirror of ``upipe_mlp_cfg``."""
+
+    _fields_ = [("L", ctypes.c_int64), ("D", ctypes.c_int32), ("F", ctypes.c_int32), ("T", ctypes.c_int32)]
+
+
+class CeCfg(ctypes.Structure):
+    """Mirror of ``upipe_ce_cfg``."""
+
+    _fields_ = [("L", ctypes.c_int64), ("D", ctypes.c_int32), ("V", ctypes.c_int32), ("T", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -124,6 +142,17 @@ def lib() -> ctypes.CDLL:
         L.upipe_attn_core_bwd.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_attn_core_bwd_noalloc.restype = ctypes.c_int
         L.upipe_attn_core_bwd_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P]
+        mcfg, ccfg = ctypes.POINTER(MlpCfg), ctypes.POINTER(CeCfg)
+        L.upipe_mlp_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_mlp_workspace_bytes.argtypes = [mcfg, ctypes.c_int]
+        L.upipe_mlp_fwd.restype = ctypes.c_int
+        L.upipe_mlp_fwd.argtypes = [mcfg, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_mlp_bwd.restype = ctypes.c_int
+        L.upipe_mlp_bwd.argtypes = [mcfg, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.upipe_ce_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_ce_workspace_bytes.argtypes = [ccfg]
+        L.upipe_ce_fwd_bwd.restype = ctypes.c_int
+        L.upipe_ce_fwd_bwd.argtypes = [ccfg, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_offload_async.restype = ctypes.c_int
         L.upipe_offload_async.argtypes = [P, P, ctypes.c_size_t, P]
         L.upipe_prefetch_async.restype = ctypes.c_int
@@ -483,3 +512,97 @@ def core_backward(cfg: Config, q, k, v, o, lse, do):
     dv = torch.empty_like(v)
     attn_core_bwd(cfg, q, k, v, o, lse, do, dq, dk, dv)
     return dq, dk, dv
+
+
+# ------------------------------------------- sequence-tiled MLP and loss
+
+def mlp_workspace_bytes(L: int, D: int, F: int, T: int, pass_: int) -> int:
+    c = MlpCfg(L, D, F, T)
+    return int(lib().upipe_mlp_workspace_bytes(ctypes.byref(c), pass_))
+
+
+def ce_workspace_bytes(L: int, D: int, V: int, T: int) -> int:
+    c = CeCfg(L, D, V, T)
+    return int(lib().upipe_ce_workspace_bytes(ctypes.byref(c)))
+
+
+def _tile_ws(need, ws, device):
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    _expect_ws(ws, need)
+    return ws, ws.numel() * ws.element_size()
+
+
+def mlp_fwd(x, Wgu, Wd, y, T, ws=None, stream=None):
+    """upipe_mlp_fwd: x [L, D], Wgu [2F, D] (gate rows, then up rows),
+    Wd [D, F], y [L, D] (written), all bf16; T rows per tile."""
+    L, D = x.shape
+    F = Wd.shape[1]
+    _expect(x, (L, D), torch.bfloat16, "x")
+    _expect(Wgu, (2 * F, D), torch.bfloat16, "Wgu")
+    _expect(Wd, (D, F), torch.bfloat16, "Wd")
+    _expect(y, (L, D), torch.bfloat16, "y")
+    _on_device(x=x, Wgu=Wgu, Wd=Wd, y=y)
+    ws, nbytes = _tile_ws(mlp_workspace_bytes(L, D, F, T, 0), ws, x.device)
+    c = MlpCfg(L, D, F, T)
+    _check(lib().upipe_mlp_fwd(ctypes.byref(c), _ptr(x), _ptr(Wgu), _ptr(Wd), _ptr(y), _ptr(ws), nbytes,
+                               _stream(stream)), "upipe_mlp_fwd")
+
+
+def mlp_bwd(x, Wgu, Wd, dy, dx, dWgu, dWd, T, ws=None, stream=None):
+    """upipe_mlp_bwd: dy, dx [L, D] bf16; dWgu [2F, D], dWd [D, F] fp32."""
+    L, D = x.shape
+    F = Wd.shape[1]
+    _expect(x, (L, D), torch.bfloat16, "x")
+    _expect(Wgu, (2 * F, D), torch.bfloat16, "Wgu")
+    _expect(Wd, (D, F), torch.bfloat16, "Wd")
+    _expect(dy, (L, D), torch.bfloat16, "dy")
+    _expect(dx, (L, D), torch.bfloat16, "dx")
+    _expect(dWgu, (2 * F, D), torch.float32, "dWgu")
+    _expect(dWd, (D, F), torch.float32, "dWd")
+    _on_device(x=x, Wgu=Wgu, Wd=Wd, dy=dy, dx=dx, dWgu=dWgu, dWd=dWd)
+    ws, nbytes = _tile_ws(mlp_workspace_bytes(L, D, F, T, 1), ws, x.device)
+    c = MlpCfg(L, D, F, T)
+    _check(lib().upipe_mlp_bwd(ctypes.byref(c), _ptr(x), _ptr(Wgu), _ptr(Wd), _ptr(dy), _ptr(dx), _ptr(dWgu),
+                               _ptr(dWd), _ptr(ws), nbytes, _stream(stream)), "upipe_mlp_bwd")
+
+
+def ce_fwd_bwd(h, W, labels, scale, loss, dh, dW, T, ws=None, stream=None):
+    """upipe_ce_fwd_bwd: h [L, D] bf16, W [V, D] bf16, labels [L] int32,
+    loss [L] fp32, dh [L, D] bf16, dW [V, D] fp32 (written)."""
+    L, D = h.shape
+    V = W.shape[0]
+    _expect(h, (L, D), torch.bfloat16, "h")
+    _expect(W, (V, D), torch.bfloat16, "W")
+    _expect(labels, (L,), torch.int32, "labels")
+    _expect(loss, (L,), torch.float32, "loss")
+    _expect(dh, (L, D), torch.bfloat16, "dh")
+    _expect(dW, (V, D), torch.float32, "dW")
+    _on_device(h=h, W=W, labels=labels, loss=loss, dh=dh, dW=dW)
+    ws, nbytes = _tile_ws(ce_workspace_bytes(L, D, V, T), ws, h.device)
+    c = CeCfg(L, D, V, T)
+    _check(lib().upipe_ce_fwd_bwd(ctypes.byref(c), _ptr(h), _ptr(W), _ptr(labels), float(scale), _ptr(loss),
+                                  _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _stream(stream)), "upipe_ce_fwd_bwd")
+
+
+def mlp_forward(x, Wgu, Wd, T):
+    y = torch.empty_like(x)
+    mlp_fwd(x, Wgu, Wd, y, T)
+    return y
+
+
+def mlp_backward(x, Wgu, Wd, dy, T):
+    dx = torch.empty_like(x)
+    dWgu = torch.empty(Wgu.shape, dtype=torch.float32, device=x.device)
+    dWd = torch.empty(Wd.shape, dtype=torch.float32, device=x.device)
+    mlp_bwd(x, Wgu, Wd, dy, dx, dWgu, dWd, T)
+    return dx, dWgu, dWd
+
+
+def ce_loss(h, W, labels, scale, T):
+    """Returns (loss [L] fp32, dh [L, D] bf16, dW [V, D] fp32)."""
+    loss = torch.empty(h.shape[0], dtype=torch.float32, device=h.device)
+    dh = torch.empty_like(h)
+    dW = torch.empty(W.shape, dtype=torch.float32, device=h.device)
+    ce_fwd_bwd(h, W, labels, scale, loss, dh, dW, T)
+    return loss, dh, dW

@@ -290,6 +290,67 @@ int upipe_offload_async(void* host_dst, const void* dev_src, size_t bytes, void*
 int upipe_prefetch_async(void* dev_dst, const void* host_src, size_t bytes, void* stream);
 int upipe_copies_join(void* stream);
 
+/* Sequence-tiled MLP and loss around the attention layer ("Untied Ulysses
+ * Pushes Llama-3-8B Training to 5 Million Tokens", paragraph on Arctic Long
+ * Sequence Training: the MLPs and the loss need no buffer that spans the
+ * whole sequence; they are computed in tiles along the sequence axis).
+ * Each call walks the L rows in tiles of T rows and keeps only one tile's
+ * intermediates in the workspace, so their memory scales with T, not L.
+ * Weight gradients are carried in place across tiles in a fixed fp32 order:
+ * every T (a multiple of 128) returns the same bits as T >= L.
+ *
+ * SwiGLU MLP: y = (silu(x Wg^T) * (x Wu^T)) Wd^T, silu(g) = g sigmoid(g),
+ * no biases (the MLP of the Llama-3 and Qwen models the pages train).
+ *   L        rows (tokens)                 D  model width, multiple of 128
+ *   F        hidden width, multiple of 128 T  rows per tile, multiple of 128 */
+typedef struct upipe_mlp_cfg {
+  int64_t L;
+  int32_t D;
+  int32_t F;
+  int32_t T;
+} upipe_mlp_cfg;
+
+/* Workspace bytes (pass 0 forward: H [T, F] bf16; pass 1 backward: H, dH
+ * [T, F] and [dG | dU] [T, 2F], bf16).  0 for an invalid configuration.   */
+size_t upipe_mlp_workspace_bytes(const upipe_mlp_cfg* cfg, int pass);
+
+/*   x    [L, D] bf16                Wgu [2F, D] bf16: the F gate rows, then the F up rows
+ *   Wd   [D, F] bf16                y   [L, D] bf16 (written)             */
+int upipe_mlp_fwd(const upipe_mlp_cfg* cfg, const uint16_t* x, const uint16_t* Wgu, const uint16_t* Wd, uint16_t* y,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Gradients of sum(y * dy); the forward is recomputed per tile.
+ *   dy   [L, D] bf16                dx [L, D] bf16 (written)
+ *   dWgu [2F, D] fp32, dWd [D, F] fp32 (written, not accumulated)
+ * Intermediates H, dH = dy Wd and [dG | dU] are stored as bf16.           */
+int upipe_mlp_bwd(const upipe_mlp_cfg* cfg, const uint16_t* x, const uint16_t* Wgu, const uint16_t* Wd,
+                  const uint16_t* dy, uint16_t* dx, float* dWgu, float* dWd, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Cross-entropy of the LM head, loss and gradients in one call:
+ * z = h W^T (fp32), loss_i = logsumexp(z_i) - z_i[label_i], and the
+ * gradients of sum_i scale * loss_i.
+ *   L, D (multiple of 128), V vocabulary (multiple of 128), T as above    */
+typedef struct upipe_ce_cfg {
+  int64_t L;
+  int32_t D;
+  int32_t V;
+  int32_t T;
+} upipe_ce_cfg;
+
+/* Workspace bytes: the logits of one tile [T, V] fp32 and dZ [T, V] bf16. */
+size_t upipe_ce_workspace_bytes(const upipe_ce_cfg* cfg);
+
+/*   h      [L, D] bf16              W [V, D] bf16
+ *   labels [L] int32: a negative label ignores the token (loss 0, no
+ *          gradient); a label >= V gives a NaN loss and no gradient
+ *   scale  finite; e.g. 1 / (number of non-negative labels) for the mean
+ *   loss   [L] fp32 (written)       dh [L, D] bf16 (written)
+ *   dW     [V, D] fp32 (written, not accumulated)
+ * dZ = scale (softmax(z) - onehot) enters dh = dZ W and dW = dZ^T h as bf16. */
+int upipe_ce_fwd_bwd(const upipe_ce_cfg* cfg, const uint16_t* h, const uint16_t* W, const int32_t* labels,
+                     float scale, float* loss, uint16_t* dh, float* dW, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the device status word of
  * the current device.  Returns UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT if a
  * bounded wait of any earlier call ran out, or UPIPE_ERR_CUDA.              */
@@ -320,7 +381,11 @@ int upipe_debug_wait_timeout(uint64_t limit_ns, void* stream);
 #define UPIPE_KIND_DX_GEMM 9
 #define UPIPE_KIND_DELTA 10
 #define UPIPE_KIND_ZERO_ROWS 11
-#define UPIPE_KIND_COUNT 12
+#define UPIPE_KIND_ALST_GU 12     /* MLP gate/up GEMM with the SwiGLU epilogue (forward and backward) */
+#define UPIPE_KIND_ALST_GEMM 13   /* MLP and loss GEMMs with one output per row: y, dH, dx, logits, dh */
+#define UPIPE_KIND_ALST_WGRAD 14  /* MLP and loss weight gradients, carried across sequence tiles */
+#define UPIPE_KIND_CE_ROWS 15     /* softmax rows of the loss */
+#define UPIPE_KIND_COUNT 16
 int64_t upipe_launch_count(void);
 void upipe_profile_enable(int on);
 int upipe_profile_read(double* ms, int64_t* launches, int n);

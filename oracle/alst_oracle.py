@@ -67,11 +67,13 @@ def mlp_fwd(x, Wgu, Wd, bf16_operands=False):
     return h @ Wd.T, h
 
 
-def mlp_bwd(x, Wgu, Wd, dy, bf16_operands=False):
+def mlp_bwd(x, Wgu, Wd, dy, bf16_operands=False, weight_grads=True):
     """dx [L, D], dWgu [2F, D], dWd [D, F]: gradient of sum(y * dy).
 
     silu'(g) = s (1 + g (1 - s)), s = sigmoid(g).  Under the precision
-    model H, dH = dy Wd and [dG | dU] enter their products as bf16.
+    model H, dH = dy Wd and [dG | dU] enter their products as bf16.  With
+    weight_grads=False only dx is formed (the other two are None), for
+    checks of sampled rows.
     """
     x = np.asarray(x, dtype=F64)
     Wgu = np.asarray(Wgu, dtype=F64)
@@ -84,11 +86,12 @@ def mlp_bwd(x, Wgu, Wd, dy, bf16_operands=False):
     silu = g * s
     h = _op(silu * u, bf16_operands)
     dh = _op(dy @ Wd, bf16_operands)
-    dWd = dy.T @ h
     dg = dh * u * (s * (1.0 + g * (1.0 - s)))
     du = dh * silu
     dgu = _op(np.concatenate([dg, du], axis=1), bf16_operands)
-    return dgu @ Wgu, dgu.T @ x, dWd
+    if not weight_grads:
+        return dgu @ Wgu, None, None
+    return dgu @ Wgu, dgu.T @ x, dy.T @ h
 
 
 def mlp_tiled(x, Wgu, Wd, dy, T, bf16_operands=False):
@@ -113,9 +116,10 @@ def mlp_tiled(x, Wgu, Wd, dy, T, bf16_operands=False):
 # Cross-entropy loss of the LM head
 # ---------------------------------------------------------------------------
 
-def ce_fwd_bwd(h, W, labels, scale, bf16_operands=False):
-    """Per-token loss [L] (0 where label < 0), dh [L, D] and dW [V, D], the
-    gradients of sum_i scale * loss_i.
+def ce_fwd_bwd(h, W, labels, scale, bf16_operands=False, weight_grad=True):
+    """Per-token loss [L] (0 where label < 0), dh [L, D] and dW [V, D] (None
+    with weight_grad=False, for checks of sampled rows), the gradients of
+    sum_i scale * loss_i.
 
     z = h W^T; loss_i = logsumexp(z_i) - z_i[label_i];
     dz_ij = scale * (softmax(z_i)_j - [j == label_i]) for a valid token, 0
@@ -134,7 +138,7 @@ def ce_fwd_bwd(h, W, labels, scale, bf16_operands=False):
     p = np.exp(z - lse[:, None])
     p[rows[valid], lab[valid]] -= 1.0
     dz = _op(np.where(valid[:, None], scale * p, 0.0), bf16_operands)
-    return loss, dz @ W, dz.T @ h
+    return loss, dz @ W, (dz.T @ h if weight_grad else None)
 
 
 def ce_tiled(h, W, labels, scale, T, bf16_operands=False):

@@ -263,3 +263,53 @@ def test_host_o_entry_points_reject_null_or_unpinned_buffers(lib):
     with pytest.raises(ValueError, match="o_host"):
         upipe.attn_fwd_host_o(cfg, x, w, wo, x, lse, torch.zeros(7, dtype=torch.bfloat16))
     assert upipe.launch_count() == n0
+
+
+# ----------------------------------------- sequence-tiled MLP and loss (host)
+
+def test_tiled_mlp_and_loss_workspace_scales_with_the_tile(lib):
+    """The MLP keeps one tile's H [T, F] (forward) or H, dH and dG|dU
+    (backward) and the loss one tile's fp32 logits and bf16 dZ [T, V]: the
+    workspace is proportional to T and independent of L."""
+    al = lambda b: (b + 1023) // 1024 * 1024
+    D, F, V = 4096, 14336, 128256
+    for T in (1024, 8192):
+        tf = T * F * 2
+        assert upipe.mlp_workspace_bytes(1 << 20, D, F, T, 0) == al(tf)
+        assert upipe.mlp_workspace_bytes(1 << 20, D, F, T, 1) == al(tf) * 2 + al(2 * tf)
+        assert upipe.mlp_workspace_bytes(3 << 20, D, F, T, 1) == upipe.mlp_workspace_bytes(1 << 20, D, F, T, 1)
+        assert upipe.ce_workspace_bytes(1 << 20, D, V, T) == al(T * V * 4) + al(T * V * 2)
+    assert upipe.mlp_workspace_bytes(1 << 20, D, F, 8192, 1) == 8 * upipe.mlp_workspace_bytes(1 << 20, D, F, 1024, 1)
+    # the oracle's own accounting of one tile's intermediates agrees
+    assert upipe.mlp_workspace_bytes(1 << 20, D, F, 8192, 1) == orc_alst().tile_bytes(8192, D, F, V)["mlp_bwd"]
+    assert upipe.ce_workspace_bytes(1 << 20, D, V, 8192) == orc_alst().tile_bytes(8192, D, F, V)["ce"]
+
+
+def orc_alst():
+    from oracle import alst_oracle
+    return alst_oracle
+
+
+@pytest.mark.parametrize("L,D,F,T", [(0, 256, 256, 128), (100, 100, 256, 128), (100, 256, 200, 128),
+                                     (100, 256, 256, 100), (100, 256, 256, 0)])
+def test_tiled_mlp_rejects_bad_shapes(lib, L, D, F, T):
+    assert upipe.mlp_workspace_bytes(L, D, F, T, 1) == 0
+    assert upipe.ce_workspace_bytes(L, D, F, T) == 0  # V takes F's place: same constraints
+    c = upipe.MlpCfg(L, D, F, T)
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.upipe_mlp_fwd(ctypes.byref(c), fake, fake, fake, fake, fake, 1 << 30, None) == upipe.UPIPE_ERR_INVALID_ARG
+
+
+def test_tiled_entry_points_reject_null_pointers_before_any_launch(lib):
+    n0 = upipe.launch_count()
+    m = upipe.MlpCfg(1024, 256, 512, 256)
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.upipe_mlp_fwd(ctypes.byref(m), fake, None, fake, fake, fake, 1 << 30, None) == -1
+    assert lib.upipe_mlp_bwd(ctypes.byref(m), fake, fake, fake, fake, fake, fake, None, fake, 1 << 30, None) == -1
+    assert lib.upipe_mlp_fwd(ctypes.byref(m), fake, fake, fake, fake, fake, 16, None) == upipe.UPIPE_ERR_WS_TOO_SMALL
+    c = upipe.CeCfg(1024, 256, 512, 256)
+    assert lib.upipe_ce_fwd_bwd(ctypes.byref(c), fake, fake, None, ctypes.c_float(1.0), fake, fake, fake, fake,
+                                1 << 32, None) == -1
+    assert lib.upipe_ce_fwd_bwd(ctypes.byref(c), fake, fake, fake, ctypes.c_float(float("inf")), fake, fake, fake,
+                                fake, 1 << 32, None) == -1
+    assert upipe.launch_count() == n0

@@ -163,6 +163,20 @@ def test_bf16_operand_mlp_rounds_exactly_the_stated_intermediates():
     assert np.array_equal(bf16_round(h), h)
 
 
+def test_row_checks_without_weight_gradients_agree():
+    x, Wgu, Wd, dy = _mlp_inputs(seed=7)
+    a = alst.mlp_bwd(x, Wgu, Wd, dy, True)
+    b = alst.mlp_bwd(x, Wgu, Wd, dy, True, weight_grads=False)
+    np.testing.assert_array_equal(a[0], b[0])
+    assert b[1] is None and b[2] is None
+    h, W, labels = _ce_inputs(seed=8)
+    a = alst.ce_fwd_bwd(h, W, labels, 0.5, True)
+    b = alst.ce_fwd_bwd(h, W, labels, 0.5, True, weight_grad=False)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    assert b[2] is None
+
+
 def test_tile_bytes_scale_with_the_tile():
     a, b = alst.tile_bytes(4096, 4096, 14336, 128256), alst.tile_bytes(65536, 4096, 14336, 128256)
     assert b["mlp_bwd"] == 16 * a["mlp_bwd"] and b["ce"] == 16 * a["ce"]
