@@ -54,6 +54,17 @@ U_SWEEP = {
     "llama3_8b_layer_L65536_U4": (32, 8, 4),
     "llama3_8b_layer_L262144_U4": (32, 8, 4),
 }
+# The MLP and vocabulary of the model family each workload's layer belongs
+# to (Llama-3-8B: F = 14336, V = 128256; Qwen2.5-32B: F = 27648, V = 152064),
+# for the sequence-tiled MLP and loss measured beside the layer; T rows per
+# tile.
+ALST_SHAPES = {
+    "qwen32b_layer_L131072_U8": dict(F=27648, V=152064, T_mlp=8192, T_ce=4096),
+    "llama3_8b_layer_L32768_U8": dict(F=14336, V=128256, T_mlp=8192, T_ce=4096),
+    "tiny_L1024_U2": dict(F=2048, V=4096, T_mlp=256, T_ce=256),
+    "llama3_8b_layer_L65536_U4": dict(F=14336, V=128256, T_mlp=8192, T_ce=4096),
+    "llama3_8b_layer_L262144_U4": dict(F=14336, V=128256, T_mlp=8192, T_ce=4096),
+}
 TARGET_FRAC_OF_BURST = 0.55
 O_MODE_NOTE = {
     "host": "kept in page-locked host memory: each chunk's O copied out during the forward and back during "
@@ -268,6 +279,75 @@ def traffic_for(kind, workload):
 
 def _bytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def alst_section(workload, w, dev, stream, steps=2):
+    """The sequence-tiled SwiGLU MLP and LM-head cross-entropy at the
+    workload's L and D and its model family's F and V: device-timed forward
+    and backward, algorithmic TFLOP/s (MLP: 6 L D F forward, 12 L D F
+    backward; loss: 6 L D V), and each call's device high-water mark next
+    to the library's workspace for one tile."""
+    from headwise_chunked_context_gb300 import synth, upipe
+    a = ALST_SHAPES[workload]
+    L, D, F, V = w["L"], w["D"], a["F"], a["V"]
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    def peak(fn):
+        """Device high-water mark of one allocating call, less its outputs."""
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        out = fn()
+        torch.cuda.synchronize(dev)
+        return torch.cuda.max_memory_allocated(dev) - base - _bytes(*out)
+
+    T = a["T_mlp"]
+    x, wgu, wd, dy = synth.mlp_inputs(L, D, F, device=dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dwgu = torch.empty(wgu.shape, dtype=torch.float32, device=dev)
+    dwd = torch.empty(wd.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(upipe.mlp_workspace_bytes(L, D, F, T, 1), dtype=torch.uint8, device=dev)
+    fwd_ms = timed(lambda: upipe.mlp_fwd(x, wgu, wd, y, T, ws, stream))
+    bwd_ms = timed(lambda: upipe.mlp_bwd(x, wgu, wd, dy, dx, dwgu, dwd, T, ws, stream))
+    del ws
+    pk_b = peak(lambda: upipe.mlp_backward(x, wgu, wd, dy, T))
+    mlp = {"L": L, "D": D, "F": F, "T": T, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "fwd_tflops": 6.0 * L * D * F / (fwd_ms / 1e3) / 1e12,
+           "bwd_tflops": 12.0 * L * D * F / (bwd_ms / 1e3) / 1e12,
+           "tflops": 18.0 * L * D * F / ((fwd_ms + bwd_ms) / 1e3) / 1e12,
+           "bwd_workspace_bytes": upipe.mlp_workspace_bytes(L, D, F, T, 1), "bwd_peak_bytes_measured": pk_b,
+           "untiled_bwd_workspace_bytes": upipe.mlp_workspace_bytes(L, D, F, L, 1),
+           "note": "backward recomputes the gate/up GEMM per tile (not counted)"}
+    del x, wgu, wd, dy, y, dx, dwgu, dwd
+    torch.cuda.empty_cache()
+    T = a["T_ce"]
+    h, wv, labels = synth.ce_inputs(L, D, V, device=dev)
+    scale = 1.0 / int((labels >= 0).sum())
+    loss = torch.empty(L, dtype=torch.float32, device=dev)
+    dh = torch.empty_like(h)
+    dw = torch.empty(wv.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(upipe.ce_workspace_bytes(L, D, V, T), dtype=torch.uint8, device=dev)
+    ce_ms = timed(lambda: upipe.ce_fwd_bwd(h, wv, labels, scale, loss, dh, dw, T, ws, stream))
+    del ws
+    pk_c = peak(lambda: upipe.ce_loss(h, wv, labels, scale, T))
+    ce = {"L": L, "D": D, "V": V, "T": T, "fwd_bwd_ms": ce_ms, "tflops": 6.0 * L * D * V / (ce_ms / 1e3) / 1e12,
+          "workspace_bytes": upipe.ce_workspace_bytes(L, D, V, T), "peak_bytes_measured": pk_c,
+          "untiled_workspace_bytes": upipe.ce_workspace_bytes(L, D, V, L),
+          "mean_loss": float(loss.sum().item() * scale)}
+    del h, wv, labels, loss, dh, dw
+    torch.cuda.empty_cache()
+    return {"mlp": mlp, "ce": ce}
 
 
 def u_sweep(w, u_list, dev, stream, x, wqkv, wo, dout, n_timed=1):
@@ -589,6 +669,10 @@ def run_upipe(args, w, world, rank, local):
     if not args.no_u_sweep:
         sweep = u_sweep(w, U_SWEEP.get(args.workload, (H, U)), dev, stream, x, wqkv, wo, dout)
         check_status("after the U sweep")
+    alst = None
+    if not args.no_alst:
+        alst = alst_section(args.workload, w, dev, stream)
+        check_status("after the tiled MLP and loss")
 
     if rank != 0:
         return
@@ -622,7 +706,7 @@ def run_upipe(args, w, world, rank, local):
                          "value": job_tflops(step_flops, other_ms, world), "steps": n_split},
         "roofline": roofline, "kernels": kernels, "profiled_step_ms": prof_step_ms,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks, "u_sweep": sweep, "offload": offload,
+        "clocks": clocks, "u_sweep": sweep, "offload": offload, "alst": alst,
     }
     print(json.dumps(line), flush=True)
 
@@ -645,6 +729,7 @@ def main():
     ap.add_argument("--cpu-sample-L", type=int, default=32768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-u-sweep", action="store_true")
+    ap.add_argument("--no-alst", action="store_true", help="skip the sequence-tiled MLP and loss measurement")
     ap.add_argument("--o-mode", default="host", choices=["host", "recompute"],
                     help="where the attention output O waits between forward and backward")
     args = ap.parse_args()

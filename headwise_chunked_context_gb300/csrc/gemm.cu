@@ -88,6 +88,7 @@ struct Layout {
   static_assert(kSmemBytes <= 227 * 1024, "gemm shared memory");
 };
 constexpr int kThreads = 192;
+constexpr int kGroupM = 16;  // m pairs per group of the tile order
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 
 template <int KIND>
@@ -446,11 +447,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool even = rank == 0;
-  // Pair tile t = (m pair t / n_pairs, slot pair t % n_pairs): consecutive
-  // pairs share the A row block.
+  // Pair tiles in groups of kGroupM m pairs: within a group the m pair
+  // varies fastest, so the ~76 pairs running at once cover at most 16 m
+  // pairs by a few n pairs, and both operand slices they read stay in L2
+  // (a plain row-major order re-streams all of B once per m pair when B
+  // exceeds L2, e.g. the MLP weights or the LM head).
   const int m_pairs = (p.m_tiles + 1) / 2;
   const int n_pairs = (p.n_tiles + 1) / 2;
   const int tiles = m_pairs * n_pairs;
+  auto pair_of = [&](int tt, int* mp, int* np) {
+    const int span = kGroupM * n_pairs;
+    const int first = (tt / span) * kGroupM;
+    const int gm = m_pairs - first < kGroupM ? m_pairs - first : kGroupM;
+    const int within = tt - (tt / span) * span;
+    *mp = first + within % gm;
+    *np = within / gm;
+  };
   // Work unit t: pair tile t % tiles over K blocks [kb_lo(t), kb_hi(t)).
   const bool ksplit = (KIND == GK_DWQKV || KIND == GK_DWO) && p.k_mid > 0 && p.k_mid < p.k_blocks;
   const int total = ksplit ? 2 * tiles : tiles;
@@ -498,10 +510,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int g = 0;  // k blocks issued so far, across tiles
       bool ok = true;
       for (int t = t0; ok && t < total; t += G) {
-        const int tt = t % tiles;
-        const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
+        int mp, np;
+        pair_of(t % tiles, &mp, &np);
+        const int mt = 2 * mp + static_cast<int>(rank);
         const int mt_ld = mt < p.m_tiles ? mt : p.m_tiles - 1;  // a missing m tile reloads the last (unused)
-        const int ns = 2 * (tt % n_pairs) + static_cast<int>(rank);
+        const int ns = 2 * np + static_cast<int>(rank);
         const bool has_b = ns < p.n_tiles;
         for (int kb = kb_lo(t); kb < kb_hi(t); ++kb, ++g) {
           const int s = g % kStages;
@@ -576,10 +589,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto prep = [&](int li, int t) {
       if constexpr (kCarry) {
         if (carry_in) {
-          const int tt = t % tiles;
-          const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
+          int mp, np;
+          pair_of(t % tiles, &mp, &np);
+          const int mt = 2 * mp + static_cast<int>(rank);
           const int m0 = mt * 128 + quad * 32;  // row of lane 0
-          const int nt0 = 2 * (tt % n_pairs);
+          const int nt0 = 2 * np;
           const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
           constexpr int kXC = Lt::kXposeChunks;
           for (int j = 0; j < nsl; ++j) {
@@ -612,9 +626,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int i = 0;
     for (int t = t0; ok && t < total; t += G, ++i) {
       const int b = i & 1;
-      const int tt = t % tiles;
-      const int mt = 2 * (tt / n_pairs) + static_cast<int>(rank);
-      const int nt0 = 2 * (tt % n_pairs);
+      int mp, np;
+      pair_of(t % tiles, &mp, &np);
+      const int mt = 2 * mp + static_cast<int>(rank);
+      const int nt0 = 2 * np;
       const int nsl = nt0 + 1 < p.n_tiles ? 2 : 1;
       const int m = mt * 128 + r;
       const bool tile_ok = mt < p.m_tiles;
@@ -623,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (tile_ok) {
         if constexpr (KIND == GK_GU || KIND == GK_GU_BWD) {
-          store_gu<KIND>(p, trow0 + b * 256, m, tt % n_pairs, valid);
+          store_gu<KIND>(p, trow0 + b * 256, m, np, valid);
         } else {
           for (int j = 0; j < nsl; ++j) {
             const uint32_t trow = trow0 + b * 256 + j * 128;
