@@ -160,3 +160,44 @@ def test_llama3_vocab_ce_L8192_sampled_rows():
     loss1, dh1, dw1 = upipe.ce_loss(h, w, labels, scale, L)
     for a, b, n in zip((loss, dh, dw), (loss1, dh1, dw1), ("loss", "dh", "dW")):
         assert torch.equal(a, b), f"T={T} vs one tile: {n} differs"
+
+
+def test_llama3_8b_mlp_and_loss_at_L2M():
+    """The MLP and loss of a Llama-3-8B block at L = 2,097,152 tokens (the
+    long-context sweep's largest length; D=4096, F=14336, V=128256).  Their
+    untiled intermediates would need ~240 GB (MLP backward) and ~1.6 TB
+    (fp32 logits and bf16 dZ) of device memory; tiles of T=16384 / 4096 rows
+    hold 1.9 GB and 3.2 GB.  Sampled rows of y, dx, loss and dh against the
+    precision-model oracle; every weight gradient finite."""
+    L, D, F, V = 1 << 21, 4096, 14336, 128256
+    Tm, Tc = 16384, 4096
+    assert upipe.mlp_workspace_bytes(L, D, F, L, 1) > 200e9
+    assert upipe.ce_workspace_bytes(L, D, V, L) > 1e12
+    x, wgu, wd, dy = synth.mlp_inputs(L, D, F, device="cuda:0")
+    y = upipe.mlp_forward(x, wgu, wd, Tm)
+    dx, dwgu, dwd = upipe.mlp_backward(x, wgu, wd, dy, Tm)
+    torch.cuda.synchronize()
+    status_ok()
+    rows = _rows(L, 8, 2)
+    X, DY = (t[rows].to("cpu", torch.float64).numpy() for t in (x, dy))
+    WGU, WD = (t.to("cpu", torch.float64).numpy() for t in (wgu, wd))
+    my, _ = alst.mlp_fwd(X, WGU, WD, bf16_operands=True)
+    mdx, _, _ = alst.mlp_bwd(X, WGU, WD, DY, bf16_operands=True, weight_grads=False)
+    assert_close(f64(y[rows]), my, "mlp y rows (L=2M)")
+    assert_close(f64(dx[rows]), mdx, "mlp dx rows (L=2M)")
+    assert torch.isfinite(dwgu).all() and torch.isfinite(dwd).all()
+    del y, dx, dwgu, dwd, dy, wgu, wd
+    torch.cuda.empty_cache()
+    _, w, labels = synth.ce_inputs(128, D, V, device="cuda:0")  # W only
+    g = torch.Generator(device="cpu")
+    g.manual_seed(23)
+    labels = torch.randint(0, V, (L,), generator=g, dtype=torch.int32).to("cuda:0")
+    scale = 1.0 / L
+    loss, dh, dw = upipe.ce_loss(x, w, labels, scale, Tc)  # x serves as the final hidden states
+    torch.cuda.synchronize()
+    status_ok()
+    W = w.to("cpu", torch.float64).numpy()
+    ml, mdh, _ = alst.ce_fwd_bwd(X, W, labels[rows].cpu().numpy(), scale, bf16_operands=True, weight_grad=False)
+    assert_close(f64(loss[rows]), ml, "ce loss rows (L=2M)")
+    assert_close(f64(dh[rows]), mdh, "ce dh rows (L=2M)")
+    assert torch.isfinite(loss).all() and torch.isfinite(dw).all()
