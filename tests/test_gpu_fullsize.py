@@ -269,13 +269,18 @@ def _assert_bit_exact(a, b, what):
 def test_llama3_8b_layer_L32768():
     """D=4096, H=32, Hkv=8, U=8 (Llama-3-8B layer shape): oracle rows, tail,
     dWo columns and one KV group's dWqkv rows, plain-definition figures;
-    U=32 bit-exact."""
+    U=32 bit-exact; O kept in host memory checked against its own model."""
     shape = synth.LLAMA8B
     inputs = synth.layer_inputs(shape)
     res = _run_layer(shape, 8, inputs)
-    _, _, Kb, Vb = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
-    _check_dwqkv_group(shape, inputs, res[3], 1, Kb, Vb)
+    kv = _check_layer_rows(shape, inputs, res, _rows(shape.L), tail=256, dwo_head=5, plain=True)
+    _check_dwqkv_group(shape, inputs, res[3], 1, kv[2], kv[3])
     _assert_bit_exact(res, _run_layer(shape, 32, inputs), "U=8 vs U=32")
+    # O kept in page-locked host memory: the forward's bits, and the backward
+    # (dx tail, one head's dWo columns) against the kept-O model
+    res_h = _run_layer(shape, 8, inputs, keep_o="host")
+    assert torch.equal(res_h[0], res[0]) and torch.equal(res_h[1], res[1])
+    _check_layer_rows(shape, inputs, res_h, _rows(shape.L, n=4), tail=128, dwo_head=21, kept_o=True, kv=kv)
 
 
 def test_qwen32b_shape_layer_L131072_u_sweep():
@@ -294,7 +299,7 @@ def test_qwen32b_shape_layer_L131072_u_sweep():
     # forward's bit for bit, the backward is checked against the kept-O model.
     res_h = _run_layer(shape, 8, inputs, keep_o="host")
     assert torch.equal(res_h[0], res8[0]) and torch.equal(res_h[1], res8[1])
-    _check_layer_rows(shape, inputs, res_h, _rows(shape.L, n=6), tail=128, dwo_head=9, kept_o=True, kv=kv)
+    _check_layer_rows(shape, inputs, res_h, _rows(shape.L, n=6), tail=128, kept_o=True, kv=kv)
     for U in (16, 64):
         _assert_bit_exact(res8, _run_layer(shape, U, inputs, peaks=peaks), f"U=8 vs U={U}")
     chunk = {}
