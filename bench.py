@@ -339,12 +339,25 @@ def alst_section(workload, w, dev, stream, steps=2):
     dw = torch.empty(wv.shape, dtype=torch.float32, device=dev)
     ws = torch.empty(upipe.ce_workspace_bytes(L, D, V, T), dtype=torch.uint8, device=dev)
     ce_ms = timed(lambda: upipe.ce_fwd_bwd(h, wv, labels, scale, loss, dh, dw, T, ws, stream))
+    # Per-kernel split of one call: the softmax rows are HBM-bound (the fp32
+    # logits read twice, dZ written in bf16: 10 bytes per logit).
+    upipe.profile_enable(True)
+    upipe.ce_fwd_bwd(h, wv, labels, scale, loss, dh, dw, T, ws, stream)
+    torch.cuda.synchronize(dev)
+    upipe.profile_enable(False)
+    prof = upipe.profile_read()
+    rows_ms, rows_n = prof["ce_rows"]
+    rows_gbs = 10.0 * L * V / (rows_ms / 1e3) / 1e9
     del ws
     pk_c = peak(lambda: upipe.ce_loss(h, wv, labels, scale, T))
     ce = {"L": L, "D": D, "V": V, "T": T, "fwd_bwd_ms": ce_ms, "tflops": 6.0 * L * D * V / (ce_ms / 1e3) / 1e12,
           "workspace_bytes": upipe.ce_workspace_bytes(L, D, V, T), "peak_bytes_measured": pk_c,
           "untiled_workspace_bytes": upipe.ce_workspace_bytes(L, D, V, L),
-          "mean_loss": float(loss.sum().item() * scale)}
+          "mean_loss": float(loss.sum().item() * scale),
+          "kernels_ms": {k: v[0] for k, v in prof.items() if v[1] > 0},
+          "rows_roofline": {"bound": "hbm", "achieved": rows_gbs, "peak": peaks()[2], "unit": "GB/s",
+                            "frac": rows_gbs / peaks()[2], "launches": rows_n,
+                            "bytes": "10 per logit: fp32 logits read twice, bf16 dZ written"}}
     del h, wv, labels, loss, dh, dw
     torch.cuda.empty_cache()
     return {"mlp": mlp, "ce": ce}
