@@ -329,6 +329,42 @@ int upipe_mlp_bwd(const upipe_mlp_cfg* cfg, const uint16_t* x, const uint16_t* W
   return UPIPE_OK;
 }
 
+int upipe_mlp_choose_t(const upipe_mlp_cfg* cfg, size_t budget_bytes, int pass) {
+  MlpShape s;
+  if ((pass < 0 || pass > 2) || !cfg) return UPIPE_ERR_INVALID_ARG;
+  upipe_mlp_cfg c = *cfg;
+  c.T = 128;
+  if (!check_mlp(&c, &s)) return UPIPE_ERR_INVALID_ARG;
+  // Bytes grow linearly with T; a tile never needs to exceed L rows.
+  const int64_t t_max = (s.L + 127) / 128 * 128;
+  const size_t per128 = mlp_plan(s, pass == 0 ? 0 : 1).total;  // T = 128: aligned to 1 KiB per buffer
+  if (per128 > budget_bytes) return UPIPE_ERR_WS_TOO_SMALL;
+  int64_t best = 128;
+  for (int64_t t = 128; t <= t_max && t <= 0x7fffff80LL; t += 128) {
+    s.T = static_cast<int>(t);
+    if (mlp_plan(s, pass == 0 ? 0 : 1).total > budget_bytes) break;
+    best = t;
+  }
+  return static_cast<int>(best);
+}
+
+int upipe_ce_choose_t(const upipe_ce_cfg* cfg, size_t budget_bytes) {
+  CeShape s;
+  if (!cfg) return UPIPE_ERR_INVALID_ARG;
+  upipe_ce_cfg c = *cfg;
+  c.T = 128;
+  if (!check_ce(&c, &s)) return UPIPE_ERR_INVALID_ARG;
+  if (ce_total(s) > budget_bytes) return UPIPE_ERR_WS_TOO_SMALL;
+  const int64_t t_max = (s.L + 127) / 128 * 128;
+  int64_t best = 128;
+  for (int64_t t = 128; t <= t_max && t <= 0x7fffff80LL; t += 128) {
+    s.T = static_cast<int>(t);
+    if (ce_total(s) > budget_bytes) break;
+    best = t;
+  }
+  return static_cast<int>(best);
+}
+
 size_t upipe_ce_workspace_bytes(const upipe_ce_cfg* cfg) {
   CeShape s;
   if (!check_ce(cfg, &s)) return 0;

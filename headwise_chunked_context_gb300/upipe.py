@@ -44,6 +44,8 @@ EXPORTS = (
     "upipe_mlp_bwd",
     "upipe_ce_workspace_bytes",
     "upipe_ce_fwd_bwd",
+    "upipe_mlp_choose_t",
+    "upipe_ce_choose_t",
     "upipe_offload_async",
     "upipe_prefetch_async",
     "upipe_copies_join",
@@ -151,6 +153,10 @@ def lib() -> ctypes.CDLL:
         L.upipe_mlp_bwd.argtypes = [mcfg, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_ce_workspace_bytes.restype = ctypes.c_size_t
         L.upipe_ce_workspace_bytes.argtypes = [ccfg]
+        L.upipe_mlp_choose_t.restype = ctypes.c_int
+        L.upipe_mlp_choose_t.argtypes = [mcfg, ctypes.c_size_t, ctypes.c_int]
+        L.upipe_ce_choose_t.restype = ctypes.c_int
+        L.upipe_ce_choose_t.argtypes = [ccfg, ctypes.c_size_t]
         L.upipe_ce_fwd_bwd.restype = ctypes.c_int
         L.upipe_ce_fwd_bwd.argtypes = [ccfg, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P]
         L.upipe_offload_async.restype = ctypes.c_int
@@ -519,6 +525,24 @@ def core_backward(cfg: Config, q, k, v, o, lse, do):
 def mlp_workspace_bytes(L: int, D: int, F: int, T: int, pass_: int) -> int:
     c = MlpCfg(L, D, F, T)
     return int(lib().upipe_mlp_workspace_bytes(ctypes.byref(c), pass_))
+
+
+def mlp_choose_t(L: int, D: int, F: int, budget_bytes: int, pass_: int = 2) -> int:
+    """Largest tile T whose MLP workspace fits the budget (upipe_mlp_choose_t)."""
+    c = MlpCfg(L, D, F, 128)
+    r = int(lib().upipe_mlp_choose_t(ctypes.byref(c), int(budget_bytes), pass_))
+    if r < 0:
+        raise UpipeError(r, "upipe_mlp_choose_t")
+    return r
+
+
+def ce_choose_t(L: int, D: int, V: int, budget_bytes: int) -> int:
+    """Largest tile T whose loss workspace fits the budget (upipe_ce_choose_t)."""
+    c = CeCfg(L, D, V, 128)
+    r = int(lib().upipe_ce_choose_t(ctypes.byref(c), int(budget_bytes)))
+    if r < 0:
+        raise UpipeError(r, "upipe_ce_choose_t")
+    return r
 
 
 def ce_workspace_bytes(L: int, D: int, V: int, T: int) -> int:

@@ -314,6 +314,13 @@ typedef struct upipe_mlp_cfg {
  * [T, F] and [dG | dU] [T, 2F], bf16).  0 for an invalid configuration.   */
 size_t upipe_mlp_workspace_bytes(const upipe_mlp_cfg* cfg, int pass);
 
+/* Largest tile T (a multiple of 128, at most L rounded up to 128) whose MLP
+ * workspace fits budget_bytes; pass 0 = forward, 1 = backward, 2 = both
+ * (the backward's, the larger).  cfg->T is ignored.  Returns T, or
+ * UPIPE_ERR_INVALID_ARG / UPIPE_ERR_WS_TOO_SMALL (not even T = 128 fits).
+ * Host arithmetic only.                                                    */
+int upipe_mlp_choose_t(const upipe_mlp_cfg* cfg, size_t budget_bytes, int pass);
+
 /*   x    [L, D] bf16                Wgu [2F, D] bf16: the F gate rows, then the F up rows
  *   Wd   [D, F] bf16                y   [L, D] bf16 (written)             */
 int upipe_mlp_fwd(const upipe_mlp_cfg* cfg, const uint16_t* x, const uint16_t* Wgu, const uint16_t* Wd, uint16_t* y,
@@ -340,6 +347,10 @@ typedef struct upipe_ce_cfg {
 
 /* Workspace bytes: the logits of one tile [T, V] fp32 and dZ [T, V] bf16. */
 size_t upipe_ce_workspace_bytes(const upipe_ce_cfg* cfg);
+
+/* Largest tile T for the loss whose workspace fits budget_bytes, as
+ * upipe_mlp_choose_t.                                                      */
+int upipe_ce_choose_t(const upipe_ce_cfg* cfg, size_t budget_bytes);
 
 /*   h      [L, D] bf16              W [V, D] bf16
  *   labels [L] int32: a negative label ignores the token (loss 0, no

@@ -313,3 +313,30 @@ def test_tiled_entry_points_reject_null_pointers_before_any_launch(lib):
     assert lib.upipe_ce_fwd_bwd(ctypes.byref(c), fake, fake, fake, ctypes.c_float(float("inf")), fake, fake, fake,
                                 fake, 1 << 32, None) == -1
     assert upipe.launch_count() == n0
+
+
+@pytest.mark.parametrize("L,D,F,V", [(131072, 5120, 27648, 152064), (1000, 256, 512, 1024), (100, 128, 128, 128)])
+def test_tile_from_a_memory_budget(lib, L, D, F, V):
+    """The largest tile whose workspace fits: at a budget equal to some T's
+    bytes that T is chosen, one byte less gives the T below it; never more
+    than L rounded up to 128; below T = 128's bytes it is an error."""
+    t_max = (L + 127) // 128 * 128
+    for T in sorted({128, min(t_max, 1024), t_max}):
+        for pass_ in (0, 1):
+            need = upipe.mlp_workspace_bytes(L, D, F, T, pass_)
+            assert upipe.mlp_choose_t(L, D, F, need, pass_) == T
+            if T > 128:
+                assert upipe.mlp_choose_t(L, D, F, need - 1, pass_) == T - 128
+        need = upipe.ce_workspace_bytes(L, D, V, T)
+        assert upipe.ce_choose_t(L, D, V, need) == T
+        if T > 128:
+            assert upipe.ce_choose_t(L, D, V, need - 1) == T - 128
+    assert upipe.mlp_choose_t(L, D, F, 1 << 62) == t_max
+    assert upipe.ce_choose_t(L, D, V, 1 << 62) == t_max
+    assert upipe.mlp_choose_t(L, D, F, upipe.mlp_workspace_bytes(L, D, F, 128, 1), 2) == 128
+    with pytest.raises(upipe.UpipeError):
+        upipe.mlp_choose_t(L, D, F, upipe.mlp_workspace_bytes(L, D, F, 128, 1) - 1, 1)
+    with pytest.raises(upipe.UpipeError):
+        upipe.ce_choose_t(L, D, V, 1000)
+    with pytest.raises(upipe.UpipeError):
+        upipe.mlp_choose_t(L, 100, F, 1 << 40)
