@@ -106,11 +106,12 @@ def _rows(L, n, seed):
     return np.unique(np.concatenate([r.integers(0, L, n), [0, L - 1]]))
 
 
-def test_llama3_8b_mlp_L32768_sampled_rows_and_columns():
-    """D=4096, F=14336 (the Llama-3-8B MLP), L=32768 in tiles of T=8192:
-    y and dx rows, dWd columns and dWgu rows against the precision-model
-    oracle, computed one by one; T=32768 (one tile) gives identical bits."""
-    L, D, F, T = 32768, 4096, 14336, 8192
+@pytest.mark.parametrize("L,D,F,T", [(32768, 4096, 14336, 8192), (65536, 5120, 27648, 16384)])
+def test_full_size_mlp_sampled_rows_and_columns(L, D, F, T):
+    """The Llama-3-8B MLP (D=4096, F=14336) and the 32B family's (D=5120,
+    F=27648) in tiles of T rows: y and dx rows, dWd columns and dWgu rows
+    against the precision-model oracle, computed one by one; one tile of all
+    L rows gives identical bits."""
     x, wgu, wd, dy = synth.mlp_inputs(L, D, F, device="cuda:0")
     y = upipe.mlp_forward(x, wgu, wd, T)
     dx, dwgu, dwd = upipe.mlp_backward(x, wgu, wd, dy, T)
@@ -140,11 +141,12 @@ def test_llama3_8b_mlp_L32768_sampled_rows_and_columns():
         assert torch.equal(a, b), f"T={T} vs one tile: {n} differs"
 
 
-def test_llama3_vocab_ce_L8192_sampled_rows():
-    """D=4096, V=128256 (the Llama-3 vocabulary), L=8192 in tiles of T=2048:
-    loss and dh rows against the oracle; T=8192 (one tile) gives identical
-    bits for loss, dh and dW."""
-    L, D, V, T = 8192, 4096, 128256, 2048
+@pytest.mark.parametrize("L,D,V,T", [(8192, 4096, 128256, 2048), (4096, 5120, 152064, 1024)])
+def test_full_vocabulary_ce_sampled_rows(L, D, V, T):
+    """The Llama-3 vocabulary (V=128256, D=4096) and the 32B family's
+    (V=152064, D=5120) in tiles of T rows: loss and dh rows against the
+    oracle; one tile of all L rows gives identical bits for loss, dh and
+    dW."""
     h, w, labels = synth.ce_inputs(L, D, V, device="cuda:0")
     scale = 1.0 / int((labels >= 0).sum())
     loss, dh, dw = upipe.ce_loss(h, w, labels, scale, T)
