@@ -300,6 +300,7 @@ def test_qwen32b_shape_layer_L131072_u_sweep():
     res_h = _run_layer(shape, 8, inputs, keep_o="host")
     assert torch.equal(res_h[0], res8[0]) and torch.equal(res_h[1], res8[1])
     _check_layer_rows(shape, inputs, res_h, _rows(shape.L, n=6), tail=128, kept_o=True, kv=kv)
+    _assert_bit_exact(res_h, _run_layer(shape, 16, inputs, keep_o="host"), "O in host memory, U=8 vs U=16")
     for U in (16, 64):
         _assert_bit_exact(res8, _run_layer(shape, U, inputs, peaks=peaks), f"U=8 vs U={U}")
     chunk = {}
