@@ -98,3 +98,42 @@ def test_emulated_ranks_sharing_a_kv_head():
     assert torch.equal(o, ro) and torch.equal(lse, rlse) and torch.equal(dq, rdq)
     assert_close(f64(dk), f64(rdk), "dk (summed across ranks)")
     assert_close(f64(dv), f64(rdv), "dv (summed across ranks)")
+
+
+@pytest.mark.parametrize("L,H,Hkv,U", [(1024, 8, 2, 4), (640, 16, 4, 8), (512, 8, 2, 2)])
+def test_chunk_loop_with_the_gpu_core_on_one_nccl_rank(L, H, Hkv, U):
+    """untied_ulysses.forward / backward with this library's kernels as the
+    core, over NCCL with a world of one rank (each all-to-all is a copy):
+    the chunk loop returns the single-GPU core's O, LSE and dQ bits, and dK
+    / dV within the tolerance (U < g sums a KV head's chunk partials in
+    fp32) or bit for bit (U >= g)."""
+    import os
+    import socket
+    import torch.distributed as dist
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda:0"))
+    try:
+        q, k, v, do = (t.to("cuda:0") for t in synth.core_inputs(L, H, Hkv))
+        core_fwd, core_bwd = uu.gpu_core()
+        o, lse = uu.forward(q, k, v, H, Hkv, U, core_fwd)
+        dq, dk, dv = uu.backward(q, k, v, o, lse, do, H, Hkv, U, core_bwd)
+        torch.cuda.synchronize()
+        status_ok()
+        cfg = upipe.Config(L=L, H=H, Hkv=Hkv, U=U)
+        ro, rlse = upipe.core_forward(cfg, q, k, v)
+        rdq, rdk, rdv = upipe.core_backward(cfg, q, k, v, ro, rlse, do)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ro) and torch.equal(dq, rdq)
+        for c in uu.plan(H, Hkv, U, 1):
+            assert torch.equal(lse[c.c], rlse[list(c.q_heads[0])])
+        if U >= H // Hkv:
+            assert torch.equal(dk.bfloat16(), rdk) and torch.equal(dv.bfloat16(), rdv)
+        else:
+            assert_close(f64(dk), f64(rdk), "dk (chunk partials summed in fp32)")
+            assert_close(f64(dv), f64(rdv), "dv (chunk partials summed in fp32)")
+    finally:
+        dist.destroy_process_group()

@@ -83,3 +83,64 @@ def test_exchange_on_two_gloo_ranks():
     while not errors.empty():
         msgs.append(errors.get())
     assert not msgs, msgs
+
+
+# ------------------------------------------- chunk loop on gloo ranks (CPU)
+
+def _oracle_core():
+    """The fp64 oracle as the attention core (the GPU path passes
+    untied_ulysses.gpu_core() instead)."""
+    import numpy as np
+    from oracle import upipe_oracle as orc
+
+    def core_fwd(q, k, v):
+        o, lse = orc.attention_core_fwd(q.numpy(), k.numpy(), v.numpy())
+        return torch.from_numpy(o), torch.from_numpy(lse)
+
+    def core_bwd(q, k, v, o, lse, do):
+        return tuple(torch.from_numpy(np.ascontiguousarray(t)) for t in
+                     orc.attention_core_bwd(q.numpy(), k.numpy(), v.numpy(), o.numpy(), lse.numpy(), do.numpy()))
+
+    return core_fwd, core_bwd
+
+
+def _loop_rank(rank, world, port, cases, errors):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import upipe_oracle as orc
+        core_fwd, core_bwd = _oracle_core()
+        for L, H, Hkv, U, d in cases:
+            g = torch.Generator().manual_seed(11)
+            q, k, v, do = (torch.randn(L, n, d, generator=g, dtype=torch.float64) for n in (H, Hkv, Hkv, H))
+            mine = list(uu.rows_of(L, world, rank))
+            o, lse = uu.forward(q[mine], k[mine], v[mine], H, Hkv, U, core_fwd)
+            dq, dk, dv = uu.backward(q[mine], k[mine], v[mine], o, lse, do[mine], H, Hkv, U, core_bwd)
+            ro, rlse = orc.attention_core_fwd(q.numpy(), k.numpy(), v.numpy())
+            rdq, rdk, rdv = orc.attention_core_bwd(q.numpy(), k.numpy(), v.numpy(), ro, rlse, do.numpy())
+            for name, got, ref in (("o", o, ro), ("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
+                err = float((got.double() - torch.from_numpy(ref)[mine]).abs().max())
+                assert err < 1e-10, f"{(L, H, Hkv, U)} {name}: max error {err:.3e}"
+            for c in uu.plan(H, Hkv, U, world):
+                ref = torch.from_numpy(rlse)[list(c.q_heads[rank])]
+                assert float((lse[c.c] - ref).abs().max()) < 1e-10, f"{(L, H, Hkv, U)} lse chunk {c.c}"
+    except AssertionError as e:
+        errors.put(f"rank {rank}: {e}")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_chunk_loop_on_two_gloo_ranks_equals_the_single_process_core():
+    """The whole Untied Ulysses chunk loop (exchanges, per-rank core, dK/dV
+    partials summed on their owners) with the fp64 oracle as the core: every
+    rank's shard of O, dQ, dK, dV and its heads' LSE equal the single-process
+    attention, for U >= g and U < g (shared KV heads across ranks and chunks)."""
+    cases = [(64, 8, 2, 4, 4), (64, 8, 2, 2, 4), (48, 8, 2, 1, 4), (32, 16, 4, 2, 8)]
+    ctx = mp.get_context("spawn")
+    errors = ctx.Queue()
+    mp.start_processes(_loop_rank, args=(2, _free_port(), cases, errors), nprocs=2, start_method="spawn")
+    msgs = []
+    while not errors.empty():
+        msgs.append(errors.get())
+    assert not msgs, msgs
