@@ -92,14 +92,25 @@ def unpack_heads(recv):
 
 # ---------------------------------------------------------------- chunk loop
 
-def _exchange(x, group):
-    """One all-to-all of a packed [P, ...] buffer: block s goes to rank s;
-    returns [P, ...] with block r from rank r."""
-    import torch
-    import torch.distributed as dist
-    out = torch.empty_like(x)
-    dist.all_to_all_single(out, x.contiguous(), group=group)
-    return out
+class _Exchange:
+    """One all-to-all of a packed [P, ...] buffer (block s goes to rank s;
+    the result holds block r from rank r), issued asynchronously: on NCCL
+    it runs on the communicator's stream beside the compute already
+    enqueued, and `result()` makes the current stream wait for it."""
+
+    def __init__(self, x, group):
+        import torch
+        import torch.distributed as dist
+        self.out = torch.empty_like(x)
+        self.work = dist.all_to_all_single(self.out, x.contiguous(), group=group, async_op=True)
+
+    def result(self):
+        self.work.wait()
+        return self.out
+
+
+def _to_heads(x, heads, group):
+    return _Exchange(pack_heads(x, heads), group)
 
 
 def forward(q, k, v, H, Hkv, U, core_fwd, group=None):
@@ -108,52 +119,90 @@ def forward(q, k, v, H, Hkv, U, core_fwd, group=None):
     the chunk's KV heads change) go from sequence to heads, the rank runs
     core_fwd(q [L, U, d], k, v [L, kv, d]) -> (o [L, U, d], lse [U, L]) on
     its U heads over the whole sequence, and O comes back to sequence shards.
-    Returns (o [n, H, d], lse) with lse[c] the [U, L] LSE of this rank's
-    heads in chunk c (kept by the head owner for the backward)."""
+    The next chunk's exchanges are issued before this chunk's attention, and
+    a chunk's O is collected only after the next chunk's attention, so that
+    on GPUs the exchanges run beside the attention (at most two chunks'
+    exchange buffers live at once: memory stays proportional to U).  Returns (o [n, H, d], lse) with lse[c]
+    the [U, L] LSE of this rank's heads in chunk c (kept by the head owner
+    for the backward)."""
     import torch
     import torch.distributed as dist
     P = dist.get_world_size(group)
-    r = dist.get_rank(group)
+    chunks = plan(H, Hkv, U, P)
+
+    def issue(c):
+        kvx = tuple(_to_heads(t, c.kv_heads, group) for t in (k, v)) if c.kv_new else None
+        return _to_heads(q, c.q_heads, group), kvx
+
     o = torch.empty_like(q)
+
+    def land(done):  # O of a finished chunk into this rank's rows
+        c, ox = done
+        o[:, [h for hs in c.q_heads for h in hs]] = unpack_heads(ox.result())
+
     lse, kv = {}, None
-    for c in plan(H, Hkv, U, P):
-        qf = unpack_sequence(_exchange(pack_heads(q, c.q_heads), group))
-        if c.kv_new:
-            kv = tuple(unpack_sequence(_exchange(pack_heads(t, c.kv_heads), group)) for t in (k, v))
-        o_c, lse[c.c] = core_fwd(qf.contiguous(), kv[0].contiguous(), kv[1].contiguous())
-        heads = [h for hs in c.q_heads for h in hs]
-        o[:, heads] = unpack_heads(_exchange(pack_rows(o_c, P), group))
+    pending, back = issue(chunks[0]), None
+    for i, c in enumerate(chunks):
+        qx, kvx = pending
+        if i + 1 < len(chunks):
+            pending = issue(chunks[i + 1])
+        qf = unpack_sequence(qx.result()).contiguous()
+        if kvx is not None:
+            kv = tuple(unpack_sequence(x.result()).contiguous() for x in kvx)
+        o_c, lse[c.c] = core_fwd(qf, kv[0], kv[1])
+        if back is not None:  # the previous chunk's O has had this chunk's attention to arrive
+            land(back)
+        back = (c, _Exchange(pack_rows(o_c, P), group))
+    land(back)
     return o, lse
 
 
 def backward(q, k, v, o, lse, do, H, Hkv, U, core_bwd, group=None):
     """Gradients of this rank's shards: dq [n, H, d], dk, dv [n, Hkv, d]
-    (sums in fp32, or the shards' dtype if wider; see below).  Per chunk: Q, O, dO (and K/V when they change)
-    go from sequence to heads, core_bwd(q, k, v, o, lse, do) -> (dq, dk, dv)
-    runs on this rank's heads, dQ comes back to sequence shards, and dK/dV
-    come back to the sequence shards of their KV heads, where the partials
-    of ranks (U < g: several ranks' query heads read one KV head) and of
-    chunks (U < g: a KV head serves several chunks) are summed in fp32."""
+    (sums in fp32, or the shards' dtype if wider).  Per chunk: Q, O, dO (and
+    K/V when they change) go from sequence to heads, core_bwd(q, k, v, o,
+    lse, do) -> (dq, dk, dv) runs on this rank's heads, dQ comes back to
+    sequence shards, and dK/dV come back to the sequence shards of their KV
+    heads, where the partials of ranks (U < g: several ranks' query heads
+    read one KV head) and of chunks (U < g: a KV head serves several chunks)
+    are summed.  The next chunk's exchanges are issued before this chunk's
+    attention, as in the forward."""
     import torch
     import torch.distributed as dist
     P = dist.get_world_size(group)
-    dq = torch.empty_like(do)
+    chunks = plan(H, Hkv, U, P)
     acc_t = torch.promote_types(k.dtype, torch.float32)  # fp32 for bf16 shards, wider inputs keep theirs
+    dq = torch.empty_like(do)
     dk = torch.zeros(k.shape, dtype=acc_t, device=k.device)
     dv = torch.zeros(v.shape, dtype=acc_t, device=v.device)
-    kv = None
-    for c in plan(H, Hkv, U, P):
-        qf, of, dof = (unpack_sequence(_exchange(pack_heads(t, c.q_heads), group)).contiguous() for t in (q, o, do))
-        if c.kv_new:
-            kv = tuple(unpack_sequence(_exchange(pack_heads(t, c.kv_heads), group)).contiguous() for t in (k, v))
-        dq_c, dk_c, dv_c = core_bwd(qf, kv[0], kv[1], of, lse[c.c], dof)
-        heads = [h for hs in c.q_heads for h in hs]
-        dq[:, heads] = unpack_heads(_exchange(pack_rows(dq_c, P), group))
+
+    def issue(c):
+        kvx = tuple(_to_heads(t, c.kv_heads, group) for t in (k, v)) if c.kv_new else None
+        return tuple(_to_heads(t, c.q_heads, group) for t in (q, o, do)), kvx
+
+    def land(done):  # a finished chunk's gradients into this rank's shards
+        c, (dqx, dkx, dvx) = done
+        dq[:, [h for hs in c.q_heads for h in hs]] = unpack_heads(dqx.result())
         kv_heads = [h for hs in c.kv_heads for h in hs]
-        for acc, part in ((dk, dk_c), (dv, dv_c)):
-            back = unpack_heads(_exchange(pack_rows(part, P), group)).to(acc_t)
+        for acc, x in ((dk, dkx), (dv, dvx)):
+            part = unpack_heads(x.result()).to(acc_t)
             for j, h in enumerate(kv_heads):
-                acc[:, h] += back[:, j]
+                acc[:, h] += part[:, j]
+
+    kv = None
+    pending, back = issue(chunks[0]), None
+    for i, c in enumerate(chunks):
+        qx, kvx = pending
+        if i + 1 < len(chunks):
+            pending = issue(chunks[i + 1])
+        qf, of, dof = (unpack_sequence(x.result()).contiguous() for x in qx)
+        if kvx is not None:
+            kv = tuple(unpack_sequence(x.result()).contiguous() for x in kvx)
+        dq_c, dk_c, dv_c = core_bwd(qf, kv[0], kv[1], of, lse[c.c], dof)
+        if back is not None:
+            land(back)
+        back = (c, tuple(_Exchange(pack_rows(t, P), group) for t in (dq_c, dk_c, dv_c)))
+    land(back)
     return dq, dk, dv
 
 
