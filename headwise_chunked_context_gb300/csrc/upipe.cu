@@ -78,7 +78,8 @@ struct Plan {
 enum OMode {
   kOWorkspace = 0,  // O_c lives in the workspace; the backward recomputes it
   kODevice = 1,     // the caller's o_saved [L, H*128] holds every chunk's O
-  kOHost = 2,       // page-locked host memory holds it; two chunk buffers stage the copies
+  kOHost = 2,       // page-locked host memory holds it; chunk buffers stage the copies
+                    // (three in the forward, two in the backward)
 };
 
 // LSE/Delta records of the backward: per head of the chunk and 64-query
@@ -101,7 +102,7 @@ Plan make_plan(const Shape& s, int pass, bool core, int o_mode) {
     p.rope = L * 64 * sizeof(float2);
     p.qkv = (s.U + 2 * s.kvc) * slot;
     if (o_mode == kOWorkspace) p.o = s.U * slot;
-    if (o_mode == kOHost) p.o = 2 * s.U * slot;
+    if (o_mode == kOHost) p.o = (pass == 0 ? 3 : 2) * s.U * slot;
     if (s.nch > 1) p.carry32 = L * s.D * 4;
     if (pass == 1) {
       p.dO = s.U * slot;
@@ -298,12 +299,12 @@ int launch_attn_bwd_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 // Copy streams of the activation offload: one per direction and device,
 // created on first use, with an event to order each batch of copies after
 // the caller's stream and one per direction to join them back.  o_ready and
-// o_done[2] order the layer entries' copies of O to and from host memory
+// o_done[3] order the layer entries' copies of O to and from host memory
 // (o_done[b]: the last copy through chunk buffer b).
 struct Copier {
   cudaStream_t d2h = nullptr, h2d = nullptr;
   cudaEvent_t after = nullptr, done_d2h = nullptr, done_h2d = nullptr;
-  cudaEvent_t o_ready = nullptr, o_done[2] = {nullptr, nullptr};
+  cudaEvent_t o_ready = nullptr, o_done[3] = {nullptr, nullptr, nullptr};
 };
 Copier g_copier[kMaxDev];
 std::mutex g_copier_mu;
@@ -321,7 +322,7 @@ int copier(Copier** out) {
     if (!c.h2d && cudaStreamCreateWithPriority(&c.h2d, cudaStreamNonBlocking, least) != cudaSuccess)
       return UPIPE_ERR_CUDA;
     if (!c.after && cudaEventCreateWithFlags(&c.after, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
-    for (cudaEvent_t* e : {&c.done_d2h, &c.o_ready, &c.o_done[0], &c.o_done[1]})
+    for (cudaEvent_t* e : {&c.done_d2h, &c.o_ready, &c.o_done[0], &c.o_done[1], &c.o_done[2]})
       if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
     if (cudaEventCreateWithFlags(&c.done_h2d, cudaEventDisableTiming) != cudaSuccess) return UPIPE_ERR_CUDA;
   }
@@ -427,8 +428,14 @@ int layer_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, con
   const int64_t ld_o = o_saved ? static_cast<int64_t>(s.H) * 128 : static_cast<int64_t>(s.U) * 128;
   const size_t o_chunk_elems = static_cast<size_t>(L) * s.U * 128;  // one chunk buffer of O
   UPIPE_MAP(map2d(&m_o, obuf, ld_o, L, ld_o, 128));
-  CUtensorMap m_o1;  // host mode: the second chunk buffer
-  if (o_host) UPIPE_MAP(map2d(&m_o1, obuf + o_chunk_elems, ld_o, L, ld_o, 128));
+  // Host mode: three chunk buffers, so a chunk's copy to host has two
+  // chunks' compute to finish before its buffer is reused.
+  CUtensorMap m_ob[3];
+  m_ob[0] = m_o;
+  if (o_host) {
+    UPIPE_MAP(map2d(&m_ob[1], obuf + o_chunk_elems, ld_o, L, ld_o, 128));
+    UPIPE_MAP(map2d(&m_ob[2], obuf + 2 * o_chunk_elems, ld_o, L, ld_o, 128));
+  }
   UPIPE_MAP(map2d(&m_wo, Wo, static_cast<uint64_t>(s.H) * 128, s.D, static_cast<uint64_t>(s.H) * 128, 128));
 
   for (int c = 0; c < s.nch; ++c) {
@@ -451,10 +458,10 @@ int layer_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, con
     // a-3: causal attention.  A kept O is written from the final
     // probabilities (LSE first, then O from it): the same bits the
     // backward's recomputation of O produces.  O bound for host memory is
-    // the online softmax's own output, staged in chunk buffer c % 2 once
-    // the copy of chunk c - 2 has left it.
-    const int buf = o_host ? (c & 1) : 0;
-    if (o_host && c >= 2) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[buf], 0));
+    // the online softmax's own output, staged in chunk buffer c % 3 once
+    // the copy of chunk c - 3 has left it.
+    const int buf = o_host ? c % 3 : 0;
+    if (o_host && c >= 3) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[buf], 0));
     AttnFwdParams a;
     std::memset(&a, 0, sizeof(a));
     a.L = static_cast<int>(L);
@@ -498,10 +505,10 @@ int layer_fwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv, con
     o.carry = carry;
     o.carry_in = c > 0;
     o.final_out = c == s.nch - 1;
-    UPIPE_LAUNCH(UPIPE_KIND_OPROJ_GEMM, launch_gemm(GK_OPROJ, buf ? m_o1 : m_o, m_wo, o, st));
+    UPIPE_LAUNCH(UPIPE_KIND_OPROJ_GEMM, launch_gemm(GK_OPROJ, m_ob[buf], m_wo, o, st));
   }
   // Host O complete when the caller's stream passes this point.
-  if (o_host) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[(s.nch - 1) & 1], 0));
+  if (o_host) UPIPE_CU(cudaStreamWaitEvent(st, cp->o_done[(s.nch - 1) % 3], 0));
   return UPIPE_OK;
 }
 

@@ -116,7 +116,8 @@ typedef struct upipe_cfg {
  *                      recomputes it from the LSE
  *   UPIPE_O_DEVICE     upipe_attn_fwd / _bwd with o_saved given
  *   UPIPE_O_HOST       upipe_attn_fwd_host_o / _bwd_host_o: page-locked host
- *                      memory holds it; two chunk buffers in the workspace  */
+ *                      memory holds it; chunk buffers of O in the workspace
+ *                      (three in the forward, two in the backward)         */
 #define UPIPE_O_RECOMPUTE 0
 #define UPIPE_O_DEVICE 1
 #define UPIPE_O_HOST 2
@@ -190,8 +191,8 @@ int upipe_attn_bwd(const upipe_cfg* cfg, const uint16_t* x, const uint16_t* Wqkv
  * recompute go to CPU memory and are prefetched for the backward pass)
  * applied to the attention output, which the recomputing backward otherwise
  * rebuilds with a second pass over the keys.  Device memory still scales
- * with U: the workspace holds two chunk buffers of O, so that one chunk's
- * copy runs while the next chunk computes.
+ * with U: the workspace holds chunk buffers of O (three in the forward, two
+ * in the backward), so that a chunk's copy runs while later chunks compute.
  *   o_host  L*H*128 bf16 (L*H*256 bytes) of page-locked host memory
  *           (cudaHostAlloc, or cudaHostRegister'ed); chunk c's O_c [L, U*128]
  *           sits at element offset c*L*U*128, so the layout depends on U and

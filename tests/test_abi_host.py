@@ -104,8 +104,9 @@ def test_workspace_arithmetic(lib):
     fwd = al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(L * D * 4)
     assert upipe.workspace_bytes(c, 0) == fwd
     assert upipe.workspace_bytes(c, 0, o_mode=upipe.O_DEVICE) == fwd - al(U * slot)
-    # O in host memory: two chunk buffers of O in place of one
-    assert upipe.workspace_bytes(c, 0, o_mode=upipe.O_HOST) == fwd - al(U * slot) + al(2 * U * slot)
+    # O in host memory: three chunk buffers of O in the forward, two in the
+    # backward, in place of one
+    assert upipe.workspace_bytes(c, 0, o_mode=upipe.O_HOST) == fwd - al(U * slot) + al(3 * U * slot)
     assert upipe.workspace_bytes(c, 0, o_mode=3) == 0 and upipe.workspace_bytes(c, 0, o_mode=-1) == 0
     rec = U * ((L + 63) // 64) * 128 * 4  # LSE/Delta records
     bwd = (al(L * 64 * 8) + al((U + 2 * kvc) * slot) + al(U * slot) + al(U * slot) + al(rec)
