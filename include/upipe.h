@@ -20,10 +20,15 @@
  *   [Q_c|K_c|V_c] = x Wqkv[rows_c]^T, RoPE on Q_c and K_c,
  *   O_c = causal_softmax(Q_c K_c^T / sqrt(d)) V_c   (plus LSE per head),
  *   out32 += O_c Wo[:, cols_c]^T,                     out = bf16(out32).
- * The backward pass recomputes Q_c/K_c/V_c (and O_c unless the caller kept
- * it), and produces the chunk's dQ/dK/dV, its rows of dWqkv, its columns of
- * dWo and its share of dx.  Every chunk reuses one workspace region, so the
- * intermediate activation memory is proportional to U rather than H.
+ * The backward pass recomputes Q_c/K_c/V_c (and O_c unless it was kept, on
+ * the device or in host memory), and produces the chunk's dQ/dK/dV, its rows
+ * of dWqkv, its columns of dWo and its share of dx.  Every chunk reuses one
+ * workspace region, so the intermediate activation memory is proportional to
+ * U rather than H.
+ *
+ * Around the layer the library also computes, tiled along the sequence, the
+ * block's SwiGLU MLP and the LM-head cross-entropy loss (upipe_mlp_*,
+ * upipe_ce_*, below).
  *
  * Conventions (readings of points the pages leave open)
  * -----------------------------------------------------
@@ -40,8 +45,9 @@
  * Memory, ownership, streams
  * --------------------------
  *  - Every pointer is a device pointer owned by the caller, including the
- *    workspace `ws`, whose size comes from upipe_workspace_bytes().  The
- *    library allocates no device memory.
+ *    workspace `ws`, whose size comes from upipe_workspace_bytes() (or the
+ *    MLP / loss variants), except the host buffers the activation-offload
+ *    calls name as such.  The library allocates no device memory.
  *  - bf16 tensors are passed as `uint16_t*` holding bfloat16 bit patterns.
  *  - Every pointer must be 16-byte aligned; tensors are dense row-major.
  *  - Work is enqueued on `stream` (a cudaStream_t, 0 = legacy default) and
