@@ -144,3 +144,17 @@ def test_chunk_loop_on_two_gloo_ranks_equals_the_single_process_core():
     while not errors.empty():
         msgs.append(errors.get())
     assert not msgs, msgs
+
+
+def test_plan_and_shards_reject_bad_shapes():
+    with pytest.raises(ValueError):
+        uu.plan(H=8, Hkv=3, U=1, P=2)   # H % Hkv != 0
+    with pytest.raises(ValueError):
+        uu.plan(H=8, Hkv=2, U=4, P=4)   # H % (U P) != 0
+    with pytest.raises(ValueError):
+        uu.rows_of(L=10, P=4, r=0)      # L % P != 0
+    assert list(uu.rows_of(L=12, P=4, r=3)) == [9, 10, 11]
+    # every query head is owned exactly once across chunks and ranks
+    for H, Hkv, U, P in ((64, 8, 8, 8), (32, 8, 1, 4), (16, 16, 2, 2)):
+        owned = [h for c in uu.plan(H, Hkv, U, P) for hs in c.q_heads for h in hs]
+        assert sorted(owned) == list(range(H))
